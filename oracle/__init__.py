@@ -1,0 +1,154 @@
+"""fp64 CPU oracle for MLA paged decode (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package.  The CUDA library never loads it, and it loads nothing
+of the CUDA library.  The arithmetic lives in ``mla_oracle.c`` (plain C,
+double precision, OpenMP over (query token, head) pairs); this module only
+builds it with gcc and marshals numpy arrays into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_SO = os.path.join(_HERE, "libmla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``libmla_oracle.so`` next to its source (gcc, OpenMP)."""
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "mla_oracle.h"))):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int32), ("N", ctypes.c_int32), ("R", ctypes.c_int32),
+        ("L", ctypes.c_int32), ("V", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("B", ctypes.c_int32), ("T", ctypes.c_int32),
+        ("mask", ctypes.c_int32), ("window", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+        ("kv_fp8", ctypes.c_int32), ("w_fp8", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("row_offsets", ctypes.c_void_p),
+        ("pool", ctypes.c_void_p),
+        ("row_scales", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("block_table_stride", ctypes.c_int32),
+        ("cache_lens", ctypes.c_void_p),
+        ("indices", ctypes.c_void_p),
+        ("indices_stride", ctypes.c_int32),
+        ("topk_lengths", ctypes.c_void_p),
+        ("w_uk", ctypes.c_void_p), ("w_uk_scale", ctypes.c_void_p),
+        ("w_uv", ctypes.c_void_p), ("w_uv_scale", ctypes.c_void_p),
+        ("t_begin", ctypes.c_int32), ("t_end", ctypes.c_int32),
+    ]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.mla_oracle_decode.argtypes = [ctypes.POINTER(_Args), ctypes.c_void_p, ctypes.c_void_p]
+            lib.mla_oracle_decode.restype = ctypes.c_int
+            lib.mla_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.mla_oracle_e4m3_value.restype = ctypes.c_double
+            lib.mla_oracle_bf16_value.argtypes = [ctypes.c_uint16]
+            lib.mla_oracle_bf16_value.restype = ctypes.c_double
+            lib.mla_oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def e4m3_value(code: int) -> float:
+    return _load().mla_oracle_e4m3_value(code)
+
+
+def bf16_value(bits: int) -> float:
+    return _load().mla_oracle_bf16_value(bits)
+
+
+def num_threads() -> int:
+    return _load().mla_oracle_num_threads()
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def decode_raw(*, H, N, R, L, V, page_size, mask, window, scale, q, row_offsets, pool,
+               row_scales=None, block_table=None, cache_lens=None, indices=None,
+               topk_lengths=None, w_uk, w_uv, w_uk_scale=None, w_uv_scale=None,
+               kv_fp8=False, w_fp8=False, t_begin=0, t_end=None):
+    """Run the oracle on explicit arrays.  Returns (out [T,H,V] f64, lse [T,H] f64);
+    rows outside [t_begin, t_end) are NaN."""
+    lib = _load()
+    keep = []
+
+    def c(a, dt):
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a, dtype=dt)
+        keep.append(a)
+        return a
+
+    q = c(q, np.uint16)
+    T = q.shape[0]
+    row_offsets = c(row_offsets, np.uint32)
+    B = len(row_offsets) - 1
+    pool = c(pool, np.uint8 if kv_fp8 else np.uint16)
+    row_scales = c(row_scales, np.float32)
+    block_table = c(block_table, np.int32)
+    cache_lens = c(cache_lens, np.uint32)
+    indices = c(indices, np.int32)
+    topk_lengths = c(topk_lengths, np.int32)
+    w_uk = c(w_uk, np.uint8 if w_fp8 else np.uint16)
+    w_uv = c(w_uv, np.uint8 if w_fp8 else np.uint16)
+    w_uk_scale = c(w_uk_scale, np.float32)
+    w_uv_scale = c(w_uv_scale, np.float32)
+    if t_end is None:
+        t_end = T
+    args = _Args(
+        H=H, N=N, R=R, L=L, V=V, page_size=page_size, B=B, T=T, mask=mask, window=window,
+        scale=float(scale), kv_fp8=int(kv_fp8), w_fp8=int(w_fp8), q=_ptr(q),
+        row_offsets=_ptr(row_offsets), pool=_ptr(pool), row_scales=_ptr(row_scales),
+        block_table=_ptr(block_table),
+        block_table_stride=0 if block_table is None else block_table.shape[1],
+        cache_lens=_ptr(cache_lens), indices=_ptr(indices),
+        indices_stride=0 if indices is None else indices.shape[1],
+        topk_lengths=_ptr(topk_lengths), w_uk=_ptr(w_uk), w_uk_scale=_ptr(w_uk_scale),
+        w_uv=_ptr(w_uv), w_uv_scale=_ptr(w_uv_scale), t_begin=t_begin, t_end=t_end)
+    out = np.full((T, H, V), np.nan)
+    lse = np.full((T, H), np.nan)
+    rc = lib.mla_oracle_decode(ctypes.byref(args), out.ctypes.data, lse.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"mla_oracle_decode failed with code {rc}")
+    return out, lse
+
+
+def decode(problem, t_begin: int = 0, t_end=None):
+    """Run the oracle on a :class:`workloads.mla.MlaProblem` (through its compact pool)."""
+    from workloads.mla import compact_view
+    p = problem
+    pool, scales, bt, ind = compact_view(p)
+    if p.kv_fmt == "bf16":
+        pool = pool.view(np.uint16)
+    return decode_raw(
+        H=p.H, N=p.N, R=p.R, L=p.L, V=p.V, page_size=p.ps, mask=p.mask, window=p.window,
+        scale=p.scale, q=p.q, row_offsets=p.row_offsets, pool=pool, row_scales=scales,
+        block_table=bt, cache_lens=p.cache_lens, indices=ind, topk_lengths=p.topk_lengths,
+        w_uk=p.w_uk, w_uv=p.w_uv, w_uk_scale=p.w_uk_scale, w_uv_scale=p.w_uv_scale,
+        kv_fp8=p.kv_fmt == "fp8", w_fp8=p.w_fmt == "fp8", t_begin=t_begin, t_end=t_end)
