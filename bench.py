@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of MLA paged decode on one GB300 (or N independent replicas).
+
+One step = one full layer call of the library (plan -> W_uk absorb -> split-KV
+decode -> combine + W_uv) on the DeepSeek-V3-shaped bf16 workload: batch 64,
+one query token each, 128 heads, nope 128, rope 64, latent 512, v 128,
+64-token pages over a 40k-page pool, cache lengths U[1024, 8192], causal.
+Inputs are synthetic and seeded; they are resident in HBM before timing.
+
+Prints one JSON line (rank 0).  The metric is microseconds per layer call
+(lower is better); HBM GB/s and TFLOP/s of the same call, the roofline
+fraction of the decode kernel and of the whole call, the oracle's CPU time on
+a sample of the workload, and an end-to-end figure through host buffers ride
+along.
+
+--impl reference times the fp64 CPU oracle (test infrastructure, never tuned)
+on bounded samples of the same workload.  Multi-GPU runs are independent
+replicas: the path needs no exchange between GPUs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/layer, HBM GB/s and tensor TFLOP/s vs roofline (B=64,H=128,4k)"
+UNIT = "us/layer"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CPU_SAMPLE_TOKENS = 48      # oracle sample for the CPU baseline (a few seconds of wall time)
+REF_SAMPLE_TOKENS = 2       # oracle sample per step of the reference arm
+KERNEL_SOURCES = {"decode_splitkv": "mla_decode_attention_06_gb300/csrc/mla_decode_simt.cu"}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["dsv3", "long", "long_swc", "fp8", "sparse"],
+                    default="dsv3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=0)
+    return ap.parse_args()
+
+
+def make_workload(name):
+    from workloads import mla as W
+    return {"dsv3": W.config_dsv3, "long": W.config_long,
+            "long_swc": lambda: W.config_long(window=4096), "fp8": W.config_fp8,
+            "sparse": W.config_sparse}[name]()
+
+
+def workload_desc(p):
+    return (f"{p.name}: B={p.B}, T={p.T}, H={p.H}, nope={p.N}, rope={p.R}, latent={p.L}, "
+            f"v={p.V}, page={p.ps}, pool pages={p.num_pages}, kv={p.kv_fmt}, w={p.w_fmt}, "
+            f"mask={['null', 'causal', 'sliding_window_causal'][p.mask]}"
+            + (f", window={p.window}" if p.window else ""))
+
+
+def key_counts(p):
+    """Attended keys per query token (the units of the decode kernel)."""
+    import numpy as np
+    if p.sparse:
+        cnt = np.minimum(p.topk_lengths if p.topk_lengths is not None
+                         else np.full(p.B, p.indices.shape[1]), p.indices.shape[1])
+        return np.array([int((p.indices[b, :cnt[b]] >= 0).sum()) for b in range(p.B)])
+    req, pos = p.query_positions()
+    lens = p.cache_lens[req].astype(np.int64)
+    if p.mask == 0:
+        return lens
+    hi = pos + 1
+    lo = np.maximum(0, hi - p.window) if p.mask == 2 else np.zeros_like(hi)
+    return hi - lo
+
+
+def algorithmic(p):
+    """Bytes and FLOPs the call must move / compute (workspace excluded)."""
+    keys = int(key_counts(p).sum())
+    row = p.row_bytes + (4 if p.kv_fmt == "fp8" else 0)
+    kv_bytes = keys * row
+    idx_bytes = (keys * 4) if p.sparse else int(sum(math.ceil(k / p.ps) for k in key_counts(p)) * 4)
+    wb = 1 if p.w_fmt == "fp8" else 2
+    w_bytes = p.H * p.L * p.N * wb + p.H * p.V * p.L * wb
+    if p.w_fmt == "fp8":
+        w_bytes += (p.w_uk_scale.size + p.w_uv_scale.size) * 4
+    q_bytes = p.T * p.H * (p.N + p.R) * 2
+    out_bytes = p.T * p.H * p.V * 2
+    flops_attn = 2 * p.H * keys * (p.L + p.R) + 2 * p.H * keys * p.L
+    flops_proj = 2 * p.T * p.H * p.L * p.N + 2 * p.T * p.H * p.V * p.L
+    return dict(keys=keys, kv_bytes=kv_bytes, decode_bytes=kv_bytes + idx_bytes,
+                total_bytes=kv_bytes + idx_bytes + w_bytes + q_bytes + out_bytes,
+                flops=flops_attn + flops_proj, flops_attn=flops_attn)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_traffic(name):
+    """ncu DRAM bytes per launch recorded under profiles/, if the kernel source still matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, KERNEL_SOURCES[name])
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(name)
+    if not rec:
+        return None
+    with open(src, "rb") as fh:
+        sha = hashlib.sha256(fh.read()).hexdigest()
+    return rec.get("bytes_per_launch") if rec.get("source_sha256") == sha else None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": n}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(p, n_tokens, heads=None, seed_name="cpu-sample"):
+    """Times the oracle on a sample of query tokens (all heads, or the first `heads`)
+    and scales to one full layer call."""
+    import numpy as np
+    import oracle
+    from workloads import mla as W
+    oracle.build()
+    st = W.Stream(11, seed_name)
+    toks = sorted(set(int(x) for x in st.integers(0, p.T - 1, n_tokens)))
+    pp = p
+    if heads is not None and heads < p.H:
+        import dataclasses
+        pp = dataclasses.replace(p, H=heads, q=np.ascontiguousarray(p.q[:, :heads]),
+                                 w_uk=np.ascontiguousarray(p.w_uk[:heads]),
+                                 w_uv=np.ascontiguousarray(p.w_uv[:heads]),
+                                 w_uk_scale=None if p.w_uk_scale is None else np.ascontiguousarray(p.w_uk_scale[:heads]),
+                                 w_uv_scale=None if p.w_uv_scale is None else np.ascontiguousarray(p.w_uv_scale[:heads]))
+    keys = key_counts(p)
+    t0 = time.perf_counter()
+    for t in toks:
+        oracle.decode(pp, t, t + 1)
+    dt = time.perf_counter() - t0
+    # scale by attended keys: the oracle's work per token is proportional to them
+    frac = (keys[toks].sum() / keys.sum()) * (pp.H / p.H)
+    return dt / frac * 1e6, toks, oracle.num_threads(), dt
+
+
+def run_reference(args, p):
+    world, rank, local = dist_setup(args)
+    if rank != 0:
+        return
+    times = []
+    cores = None
+    for i in range(args.warmup + args.steps):
+        us, toks, cores, _ = cpu_baseline(p, REF_SAMPLE_TOKENS, seed_name=f"ref-step-{i}")
+        if i >= args.warmup:
+            times.append(us)
+    value = statistics.mean(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": workload_desc(p), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {REF_SAMPLE_TOKENS} query tokens x all heads, "
+                                   "scaled by attended keys to one layer call"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    import numpy as np
+    import torch
+
+    p = make_workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, p)
+        return
+
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+
+    from mla_decode_attention_06_gb300 import build as libbuild
+    libbuild.build()
+    import mla_decode_attention_06_gb300 as M
+    from workloads.run import device_inputs, run_gpu
+
+    d = device_inputs(p, dev)
+    ws = torch.empty(max(256, __import__("workloads.run", fromlist=["x"]).workspace_bytes(p, args.num_splits)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((p.T, p.H, p.V), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((p.T, p.H), dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(timing=False):
+        run_gpu(p, d, num_splits=args.num_splits, out=out, lse_out=lse, workspace=ws,
+                stream=stream, timing=timing)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    M.kernel_times()   # clear
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.25)
+    w0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step(timing=True)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kt, ncalls = M.kernel_times()
+    ms = statistics.mean(per_step)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    alg = algorithmic(p)
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    bf16_peak = float(peaks["bf16_tflops"])
+    us = ms * 1e3
+    call_gbs = alg["total_bytes"] / (ms * 1e-3) / 1e9
+    call_tflops = alg["flops"] / (ms * 1e-3) / 1e12
+    roof_us = max(alg["total_bytes"] / (hbm_peak * 1e9), alg["flops"] / (bf16_peak * 1e12)) * 1e6
+    dec_ms = kt.get("decode_splitkv")
+    dec_gbs = alg["decode_bytes"] / (dec_ms * 1e-3) / 1e9 if dec_ms else None
+    traffic = kernel_traffic("decode_splitkv")
+
+    line = {
+        # replicas: every rank makes one layer call per step, so the job's time per
+        # layer call is the slowest rank's step time divided by the number of ranks
+        "metric": METRIC, "value": us / world, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if p.kv_fmt == "bf16" else "e4m3->bf16", "data": "synthetic (seeded)",
+        "config": {"workload": workload_desc(p), "global_batch": p.B * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)",
+                   "num_splits": args.num_splits or "auto"},
+        "hbm_gbs": call_gbs, "tflops": call_tflops,
+        "roofline_call": {"bound": "hbm" if alg["total_bytes"] / hbm_peak >= alg["flops"] / (bf16_peak * 1e3) else "tensor",
+                          "roofline_us": roof_us, "frac": roof_us / us},
+        "roofline": {"kernel": "decode_splitkv", "bound": "hbm", "achieved": dec_gbs,
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": (dec_gbs / hbm_peak) if dec_gbs else None, "traffic": traffic,
+                     "peak_source": f"hbm_gbs of {peak_kind}",
+                     "algorithmic_bytes_per_launch": alg["decode_bytes"]},
+        "kernel_ms": {k: v for k, v in kt.items()}, "kernel_calls_timed": ncalls,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(p, d, args, dev, out, lse, ws, flush, stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        us_cpu, toks, cores, dt = cpu_baseline(p, CPU_SAMPLE_TOKENS)
+        line["cpu_baseline"] = {"value": us_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{len(toks)} of {p.T} query tokens x all {p.H} heads "
+                                          f"({dt:.1f} s wall), scaled by attended keys to one call"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def e2e(p, d, args, dev, out, lse, ws, flush, stream, world):
+    """The same call through host buffers: pinned H2D of this step's inputs (q, offsets,
+    block table, cache lengths), the call, D2H of the output."""
+    import torch
+    from workloads.run import run_gpu
+    host = {k: d[k].cpu().pin_memory() for k in ("q", "offsets", "block_table", "cache_lens", "indices", "topk")
+            if d.get(k) is not None}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dd = dict(d)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size()
+    times = []
+    n = max(10, min(args.steps, 50))
+    for i in range(n + 3):
+        flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for k, t in host.items():
+            dd[k] = d[k]
+            dd[k].copy_(t, non_blocking=True)
+        run_gpu(p, dd, num_splits=args.num_splits, out=out, lse_out=None, workspace=ws,
+                stream=stream, want_lse=False)
+        out_h.copy_(out, non_blocking=True)
+        e.record(stream)
+        e.synchronize()
+        if i >= 3:
+            times.append(s.elapsed_time(e))
+    ms = statistics.mean(times)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) multi-head latent attention
+ * (MLA) decode library, libmla_decode.so.
+ *
+ * One call computes, for every query token t of a ragged batch and every head h,
+ * the absorbed MLA decode described on the Modular MAX/Mojo API pages
+ * "mla_decode_branch_fp8" (fused steps: q_nope @ w_uk, concat with q_rope,
+ * MLA decode, raw_output @ w_uv) and "generic_flare_mla_decode_kv_cache_ragged"
+ * (Args: q, input_row_offsets, kv_collection, scale, output; Parameters:
+ * mask_str, local_window_size, sparse_mla; optional d_indices, indices_stride,
+ * topk_lengths):
+ *
+ *   q_lat[l]  = sum_n w_uk[h,l,n] q[t,h,n]                       (l < L)
+ *   s_j       = scale * ( q_lat . c_kv[row_j] + q[t,h,N:N+R] . k_rope[row_j] )
+ *   o         = softmax_j(s) . c_kv[rows]                          (latent, L wide)
+ *   out[t,h,v]= sum_l w_uv[h,v,l] o[l]
+ *   lse[t,h]  = ln sum_j exp(s_j)            (natural log of the scaled scores)
+ *
+ * Shapes use H = num_heads, N = qk_nope, R = qk_rope, L = kv_lora_rank,
+ * V = v_head, ps = page_size, B = batch (requests), T = total query tokens.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, row-major, densely packed unless a
+ *     stride argument says otherwise.  Scalars and the two structs are host memory.
+ *   - The caller owns every buffer.  The library allocates nothing: scratch space
+ *     is the caller's `workspace` (size from mla_decode_workspace_size).
+ *     `out` and `lse_out` must not alias an input or the workspace.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and the call returns without synchronising, except when
+ *     opts->flags has MLA_FLAG_DEBUG_CHECKS: then it waits for the stream and
+ *     reports what the device-side checks found.
+ *   - A cache row is [c_kv (L) ; k_rope (R)], the concat order of the absorbed
+ *     query.  cache_lens[b] counts every cached token of request b including
+ *     its query tokens: query i of a request with qlen queries sits at position
+ *     pos = cache_lens[b] - qlen + i.
+ *   - Masks (mask_str on the decode page): NULL attends keys j < cache_len,
+ *     CAUSAL keys j <= pos, SLIDING_WINDOW_CAUSAL keys pos - window < j <= pos.
+ *   - The output is fully overwritten.  A query with no key gets out = 0 and
+ *     lse = -inf.
+ *   - Page ids outside [0, num_pages) and sparse rows outside
+ *     [0, num_pages * page_size) are never dereferenced: their keys are dropped
+ *     and the device records MLA_ERR_DEVICE_CHECK (returned in debug mode).
+ *   - Return value: an mla_status_t; mla_status_string() gives its text.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,        /* NULL required pointer, bad sizes, bad mask or window */
+  MLA_ERR_UNSUPPORTED = 2,        /* shape without a kernel instance, H > 128, q_scale != NULL */
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3,
+  MLA_ERR_CUDA = 4,               /* a CUDA runtime or driver call failed */
+  MLA_ERR_DEVICE_CHECK = 5,       /* debug mode: a device-side input check failed */
+  MLA_ERR_TIMEOUT = 6             /* debug mode: a bounded device wait gave up */
+} mla_status_t;
+
+typedef enum {
+  MLA_MASK_NULL = 0,
+  MLA_MASK_CAUSAL = 1,
+  MLA_MASK_SLIDING_WINDOW_CAUSAL = 2
+} mla_mask_t;
+
+#define MLA_FLAG_DEBUG_CHECKS 1u
+/* Record a CUDA event pair around every kernel of the call; read the durations
+ * with mla_decode_kernel_times() once the stream has finished. */
+#define MLA_FLAG_KERNEL_TIMING 2u
+
+/* Problem dimensions (decode page: q [.., num_heads, q_head_size];
+ * mla_decode_branch_fp8 page: w_uk [num_heads, kv_latent_dim, qk_nope_head_dim],
+ * w_uv [num_heads, v_head_dim, kv_latent_dim]). */
+typedef struct {
+  int32_t num_heads;     /* H, 1..128 */
+  int32_t qk_nope;       /* N */
+  int32_t qk_rope;       /* R */
+  int32_t kv_lora_rank;  /* L */
+  int32_t v_head;        /* V */
+  int32_t page_size;     /* ps, tokens per cache page */
+  int32_t num_pages;     /* pages in the pool */
+} mla_dims_t;
+
+/* Call options (decode page: mask_str, local_window_size, scale, num_partitions_in). */
+typedef struct {
+  int32_t mask;          /* mla_mask_t */
+  int32_t window;        /* tokens, >= 1 for SLIDING_WINDOW_CAUSAL, ignored otherwise */
+  float scale;           /* multiplies q.k, usually 1/sqrt(N + R) */
+  int32_t num_splits;    /* KV partitions; 0 = one per pair of SMs */
+  uint32_t flags;        /* MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_KERNEL_TIMING */
+} mla_opts_t;
+
+/* Bytes of scratch a call needs for `total_q` query tokens with these dims and
+ * opts (num_splits decides the partial-result slots).  Uses the current
+ * device's SM count when opts->num_splits == 0.  Writes *bytes. */
+int mla_decode_workspace_size(const mla_dims_t* dims, const mla_opts_t* opts, int32_t batch,
+                              int32_t total_q, size_t* bytes);
+
+/* Dense bf16 decode over a paged cache (decode page: q, input_row_offsets,
+ * kv_collection; the collection is flattened to pool + block_table + cache_lens).
+ *   q                  bf16 [T, H, N+R]   (nope first, then rope)
+ *   input_row_offsets  uint32 [B+1], non-decreasing, [0] = 0, [B] = T
+ *   kv_pool            bf16 [num_pages, ps, L+R]
+ *   block_table        int32 [B, block_table_stride]: physical page of logical page p
+ *   cache_lens         uint32 [B], <= block_table_stride * ps
+ *   w_uk               bf16 [H, L, N]
+ *   w_uv               bf16 [H, V, L]
+ *   out                bf16 [T, H, V]
+ *   lse_out            float [T, H] or NULL */
+int mla_decode_paged(const mla_dims_t* dims, const mla_opts_t* opts, const void* q,
+                     const uint32_t* input_row_offsets, int32_t batch, int32_t total_q,
+                     const void* kv_pool, const int32_t* block_table, int32_t block_table_stride,
+                     const uint32_t* cache_lens, const void* w_uk, const void* w_uv, void* out,
+                     float* lse_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* FP8 latent cache (decode page: per_token_scale_rope_aware, "interleaved FP8+BF16";
+ * indexer page: K scales at head-size granularity, i.e. one fp32 scale per row;
+ * mla_decode_branch_fp8 page: w_uk_scale, w_uv_scale with block granularity).
+ *   kv_pool_fp8   bytes [num_pages, ps, L + 2R]: L e4m3 (OCP E4M3FN) c_kv codes,
+ *                 then R bf16 k_rope values; c_kv = code * kv_scales[row]
+ *   kv_scales     float [num_pages, ps]
+ *   w_uk_fp8      e4m3 [H, L, N], w_uk_scale float [H, ceil(L/128), ceil(N/128)]
+ *   w_uv_fp8      e4m3 [H, V, L], w_uv_scale float [H, ceil(V/128), ceil(L/128)]
+ *   q_scale       must be NULL (sigma_Q = 1, the decode page's default)
+ * Other arguments as mla_decode_paged. */
+int mla_decode_paged_fp8(const mla_dims_t* dims, const mla_opts_t* opts, const void* q,
+                         const uint32_t* input_row_offsets, int32_t batch, int32_t total_q,
+                         const void* kv_pool_fp8, const float* kv_scales,
+                         const int32_t* block_table, int32_t block_table_stride,
+                         const uint32_t* cache_lens, const void* w_uk_fp8,
+                         const float* w_uk_scale, const void* w_uv_fp8, const float* w_uv_scale,
+                         const float* q_scale, void* out, float* lse_out, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Sparse top-k decode (decode page: sparse_mla, d_indices, indices_stride,
+ * topk_lengths; indexer page: -1 marks an unused slot).
+ *   kv_pool        bf16 [num_pages, ps, L+R]
+ *   d_indices      int32 [B, indices_stride]: physical pool rows (page * ps + slot)
+ *                  shared by all query tokens of request b; -1 is skipped wherever
+ *                  it appears; duplicates count once per occurrence
+ *   topk_lengths   int32 [B] or NULL: slots k >= topk_lengths[b] are ignored
+ *                  (NULL: all indices_stride slots are considered)
+ * opts->mask must be MLA_MASK_NULL (no positional mask on given rows).
+ * Other arguments as mla_decode_paged. */
+int mla_decode_sparse(const mla_dims_t* dims, const mla_opts_t* opts, const void* q,
+                      const uint32_t* input_row_offsets, int32_t batch, int32_t total_q,
+                      const void* kv_pool, const int32_t* d_indices, int32_t indices_stride,
+                      const int32_t* topk_lengths, const void* w_uk, const void* w_uv,
+                      void* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* Mean per-kernel device durations (milliseconds) over the calls on the current
+ * device that set MLA_FLAG_KERNEL_TIMING since the previous read (at most the
+ * last 4096), in launch order: [0] plan, [1] W_uk absorb, [2] split-KV decode,
+ * [3] combine + W_uv.  Waits for those calls' events and clears the record.
+ * Writes min(n, 4) values; returns the number of calls averaged, 0 if none,
+ * -1 on a CUDA error.  Host-side bookkeeping only: not thread-safe. */
+int mla_decode_kernel_times(float* ms, int32_t n);
+
+/* Static text for a status code. */
+const char* mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H */

@@ -1,0 +1,326 @@
+// C ABI of libmla_decode.so: argument checks, workspace carving and the launch
+// sequence  K0 plan -> K1 absorb -> K2 split-KV decode -> K3 combine + W_uv.
+// Nothing here allocates or synchronises unless MLA_FLAG_DEBUG_CHECKS is set.
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "mla_kernels.cuh"
+
+using namespace mla;
+
+namespace {
+
+constexpr int kMaxSplits = 1 << 16;
+constexpr int kTimedKernels = 4;
+constexpr int kMaxDevices = 64;
+
+// Event sets of the timed calls made since the last read, per device
+// (created on first use, reused afterwards).
+constexpr int kMaxTimedCalls = 4096;
+struct EventSet {
+  cudaEvent_t ev[kTimedKernels + 1];
+};
+struct KernelTimer {
+  EventSet* sets = nullptr;
+  int created = 0;
+  int used = 0;      // calls recorded since the last read (saturates at kMaxTimedCalls)
+  int next = 0;      // ring position
+};
+KernelTimer g_timer[kMaxDevices];
+
+EventSet* next_event_set() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  KernelTimer& t = g_timer[dev];
+  if (!t.sets) {
+    t.sets = new (std::nothrow) EventSet[kMaxTimedCalls];
+    if (!t.sets) return nullptr;
+  }
+  const int slot = t.next;
+  if (slot >= t.created) {
+    for (auto& e : t.sets[slot].ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    t.created = slot + 1;
+  }
+  t.next = (slot + 1) % kMaxTimedCalls;
+  if (t.used < kMaxTimedCalls) ++t.used;
+  return &t.sets[slot];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const mla_dims_t* d) {
+  if (!d) return MLA_ERR_INVALID_ARG;
+  if (d->num_heads < 1 || d->qk_nope < 1 || d->qk_rope < 0 || d->kv_lora_rank < 1 || d->v_head < 1 ||
+      d->page_size < 1 || d->num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (d->num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
+  // L multiple of 16 (latent columns are split 16 per lane group), L <= 512;
+  // even row widths keep every row 4-byte aligned.
+  if (d->kv_lora_rank % 16 != 0 || d->kv_lora_rank > 512 || d->qk_rope % 2 != 0 || d->qk_nope % 2 != 0)
+    return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)d->num_pages * d->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+int resolve_splits(const mla_opts_t* o, int* K) {
+  if (o->num_splits < 0 || o->num_splits > kMaxSplits) return MLA_ERR_INVALID_ARG;
+  if (o->num_splits > 0) {
+    *K = o->num_splits;
+    return MLA_OK;
+  }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
+  *K = sms / 2 > 0 ? sms / 2 : 1;
+  return MLA_OK;
+}
+
+int check_opts(const mla_opts_t* o) {
+  if (!o) return MLA_ERR_INVALID_ARG;
+  if (o->mask < MLA_MASK_NULL || o->mask > MLA_MASK_SLIDING_WINDOW_CAUSAL) return MLA_ERR_INVALID_ARG;
+  if (o->mask == MLA_MASK_SLIDING_WINDOW_CAUSAL && o->window < 1) return MLA_ERR_INVALID_ARG;
+  if (!(o->scale == o->scale)) return MLA_ERR_INVALID_ARG;   // NaN
+  if (o->flags & ~(MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_KERNEL_TIMING)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+struct CallCommon {
+  const mla_dims_t* d;
+  const mla_opts_t* o;
+  const void* q;
+  const uint32_t* offsets;
+  int B, T;
+  KeySource ks;
+  KVFmt kv_fmt;
+  const void* kv_pool;
+  const float* kv_scales;
+  WFmt w_fmt;
+  const void *w_uk, *w_uv;
+  const float *w_uk_scale, *w_uv_scale;
+  void* out;
+  float* lse_out;
+  void* ws;
+  size_t ws_bytes;
+  cudaStream_t stream;
+};
+
+int run(const CallCommon& c) {
+  int st = check_dims(c.d);
+  if (st) return st;
+  if ((st = check_opts(c.o))) return st;
+  if (c.B < 1 || c.T < 0) return MLA_ERR_INVALID_ARG;
+  if (!c.q || !c.offsets || !c.kv_pool || !c.w_uk || !c.w_uv || !c.out || !c.ws) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c.q) || !aligned16(c.kv_pool) || !aligned16(c.w_uk) || !aligned16(c.w_uv) ||
+      !aligned16(c.out) || !aligned16(c.ws))
+    return MLA_ERR_INVALID_ARG;
+  int K = 0;
+  if ((st = resolve_splits(c.o, &K))) return st;
+  const WorkspaceLayout lay = workspace_layout(*c.d, c.T, K);
+  if (c.ws_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+
+  char* ws = static_cast<char*>(c.ws);
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws + lay.header);
+  TokenPlan* plan = reinterpret_cast<TokenPlan*>(ws + lay.plan);
+  DecodeArgs a{};
+  a.d = *c.d;
+  a.B = c.B;
+  a.T = c.T;
+  a.K = K;
+  a.mask = c.o->mask;
+  a.window = c.o->window;
+  a.scale = c.o->scale;
+  a.kv_fmt = c.kv_fmt;
+  a.kv_pool = c.kv_pool;
+  a.kv_scales = c.kv_scales;
+  a.ks = c.ks;
+  a.hdr = hdr;
+  a.hdr_mut = hdr;
+  a.plan = plan;
+  a.q_full = reinterpret_cast<const __nv_bfloat16*>(ws + lay.q_full);
+  a.o_lat = reinterpret_cast<__nv_bfloat16*>(ws + lay.o_lat);
+  a.lse_ws = reinterpret_cast<float*>(ws + lay.lse);
+  a.part_o = reinterpret_cast<float*>(ws + lay.part_o);
+  a.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
+
+  EventSet* timer = nullptr;
+  if (c.o->flags & MLA_FLAG_KERNEL_TIMING) {
+    timer = next_event_set();
+    if (!timer) return MLA_ERR_CUDA;
+  }
+  auto mark = [&](int i) {
+    return timer ? cudaEventRecord(timer->ev[i], c.stream) : cudaSuccess;
+  };
+  cudaError_t e = mark(0);
+  if (e == cudaSuccess) e = launch_plan(c.offsets, c.B, c.T, c.ks, c.o->mask, c.o->window, plan, hdr, c.stream);
+  if (e == cudaSuccess) e = mark(1);
+  if (e == cudaSuccess)
+    e = launch_absorb(*c.d, c.T, static_cast<const __nv_bfloat16*>(c.q), c.w_fmt, c.w_uk, c.w_uk_scale,
+                      reinterpret_cast<__nv_bfloat16*>(ws + lay.q_full), c.stream);
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess && c.T > 0) e = launch_decode(a, c.stream);
+  if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess)
+    e = launch_combine_uv(a, c.w_fmt, c.w_uv, c.w_uv_scale, static_cast<__nv_bfloat16*>(c.out), c.lse_out,
+                          c.stream);
+  if (e == cudaSuccess) e = mark(4);
+  if (e != cudaSuccess) {
+    std::fprintf(stderr, "mla_decode: %s\n", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  if (c.o->flags & MLA_FLAG_DEBUG_CHECKS) {
+    int status = 0;
+    if (cudaMemcpyAsync(&status, &hdr->status, sizeof(int), cudaMemcpyDeviceToHost, c.stream) != cudaSuccess ||
+        cudaStreamSynchronize(c.stream) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    if (status & kDeviceTimeout) return MLA_ERR_TIMEOUT;
+    if (status & kDeviceCheckFailed) return MLA_ERR_DEVICE_CHECK;
+  }
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_workspace_size(const mla_dims_t* dims, const mla_opts_t* opts, int32_t batch, int32_t total_q,
+                              size_t* bytes) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!opts || !bytes || batch < 1 || total_q < 0) return MLA_ERR_INVALID_ARG;
+  int K = 0;
+  if ((st = resolve_splits(opts, &K))) return st;
+  *bytes = workspace_layout(*dims, total_q, K).total;
+  return MLA_OK;
+}
+
+int mla_decode_paged(const mla_dims_t* dims, const mla_opts_t* opts, const void* q,
+                     const uint32_t* input_row_offsets, int32_t batch, int32_t total_q, const void* kv_pool,
+                     const int32_t* block_table, int32_t block_table_stride, const uint32_t* cache_lens,
+                     const void* w_uk, const void* w_uv, void* out, float* lse_out, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!dims || !block_table || !cache_lens || block_table_stride < 1) return MLA_ERR_INVALID_ARG;
+  CallCommon c{};
+  c.d = dims;
+  c.o = opts;
+  c.q = q;
+  c.offsets = input_row_offsets;
+  c.B = batch;
+  c.T = total_q;
+  c.ks = KeySource{block_table, block_table_stride, cache_lens, nullptr, 0, nullptr, dims->page_size,
+                   dims->num_pages};
+  c.kv_fmt = KVFmt::kBF16;
+  c.kv_pool = kv_pool;
+  c.w_fmt = WFmt::kBF16;
+  c.w_uk = w_uk;
+  c.w_uv = w_uv;
+  c.out = out;
+  c.lse_out = lse_out;
+  c.ws = workspace;
+  c.ws_bytes = workspace_bytes;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+int mla_decode_paged_fp8(const mla_dims_t* dims, const mla_opts_t* opts, const void* q,
+                         const uint32_t* input_row_offsets, int32_t batch, int32_t total_q,
+                         const void* kv_pool_fp8, const float* kv_scales, const int32_t* block_table,
+                         int32_t block_table_stride, const uint32_t* cache_lens, const void* w_uk_fp8,
+                         const float* w_uk_scale, const void* w_uv_fp8, const float* w_uv_scale,
+                         const float* q_scale, void* out, float* lse_out, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (q_scale) return MLA_ERR_UNSUPPORTED;
+  if (!dims || !block_table || !cache_lens || block_table_stride < 1 || !kv_scales || !w_uk_scale ||
+      !w_uv_scale)
+    return MLA_ERR_INVALID_ARG;
+  CallCommon c{};
+  c.d = dims;
+  c.o = opts;
+  c.q = q;
+  c.offsets = input_row_offsets;
+  c.B = batch;
+  c.T = total_q;
+  c.ks = KeySource{block_table, block_table_stride, cache_lens, nullptr, 0, nullptr, dims->page_size,
+                   dims->num_pages};
+  c.kv_fmt = KVFmt::kE4M3;
+  c.kv_pool = kv_pool_fp8;
+  c.kv_scales = kv_scales;
+  c.w_fmt = WFmt::kE4M3;
+  c.w_uk = w_uk_fp8;
+  c.w_uv = w_uv_fp8;
+  c.w_uk_scale = w_uk_scale;
+  c.w_uv_scale = w_uv_scale;
+  c.out = out;
+  c.lse_out = lse_out;
+  c.ws = workspace;
+  c.ws_bytes = workspace_bytes;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+int mla_decode_sparse(const mla_dims_t* dims, const mla_opts_t* opts, const void* q,
+                      const uint32_t* input_row_offsets, int32_t batch, int32_t total_q, const void* kv_pool,
+                      const int32_t* d_indices, int32_t indices_stride, const int32_t* topk_lengths,
+                      const void* w_uk, const void* w_uv, void* out, float* lse_out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!dims || !opts || !d_indices || indices_stride < 1) return MLA_ERR_INVALID_ARG;
+  if (opts->mask != MLA_MASK_NULL) return MLA_ERR_UNSUPPORTED;
+  CallCommon c{};
+  c.d = dims;
+  c.o = opts;
+  c.q = q;
+  c.offsets = input_row_offsets;
+  c.B = batch;
+  c.T = total_q;
+  c.ks = KeySource{nullptr, 0, nullptr, d_indices, indices_stride, topk_lengths, dims->page_size,
+                   dims->num_pages};
+  c.kv_fmt = KVFmt::kBF16;
+  c.kv_pool = kv_pool;
+  c.w_fmt = WFmt::kBF16;
+  c.w_uk = w_uk;
+  c.w_uv = w_uv;
+  c.out = out;
+  c.lse_out = lse_out;
+  c.ws = workspace;
+  c.ws_bytes = workspace_bytes;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return run(c);
+}
+
+int mla_decode_kernel_times(float* ms, int32_t n) {
+  int dev = 0;
+  if (!ms || n < 0 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  KernelTimer& t = g_timer[dev];
+  const int calls = t.used;
+  t.used = 0;
+  if (calls == 0) return 0;
+  double sum[kTimedKernels] = {0, 0, 0, 0};
+  for (int c = 0; c < calls; ++c) {
+    const int slot = (t.next - 1 - c + 2 * kMaxTimedCalls) % kMaxTimedCalls;
+    EventSet& es = t.sets[slot];
+    if (cudaEventSynchronize(es.ev[kTimedKernels]) != cudaSuccess) return -1;
+    for (int i = 0; i < kTimedKernels; ++i) {
+      float v = 0.f;
+      if (cudaEventElapsedTime(&v, es.ev[i], es.ev[i + 1]) != cudaSuccess) return -1;
+      sum[i] += v;
+    }
+  }
+  for (int i = 0; i < kTimedKernels && i < n; ++i) ms[i] = (float)(sum[i] / calls);
+  return calls;
+}
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_DEVICE_CHECK: return "device-side input check failed";
+    case MLA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

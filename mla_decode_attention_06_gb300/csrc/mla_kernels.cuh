@@ -1,0 +1,43 @@
+// Launchers of the device kernels (internal to libmla_decode.so).
+#pragma once
+#include "mla_common.cuh"
+
+namespace mla {
+
+// Weight / cache element formats.
+enum class WFmt { kBF16, kE4M3 };
+enum class KVFmt { kBF16, kE4M3 };
+
+struct DecodeArgs {
+  mla_dims_t d;
+  int B, T, K;                  // requests, query tokens, KV partitions
+  int mask, window;
+  float scale;
+  KVFmt kv_fmt;
+  const void* kv_pool;          // bf16 rows [L+R] or fp8 rows [L | 2R bytes]
+  const float* kv_scales;       // fp8 row scales
+  KeySource ks;
+  const PlanHeader* hdr;
+  PlanHeader* hdr_mut;
+  const TokenPlan* plan;
+  const __nv_bfloat16* q_full;  // [T, 128, L+R]
+  __nv_bfloat16* o_lat;         // [T, H, L]
+  float* lse_ws;                // [T, H]
+  float* part_o;                // [K, 2, H, L]
+  float* part_lse;              // [K, 2, H]
+};
+
+cudaError_t launch_plan(const uint32_t* offsets, int B, int T, const KeySource& ks, int mask,
+                        int window, TokenPlan* plan, PlanHeader* hdr, cudaStream_t s);
+
+cudaError_t launch_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q, WFmt wf,
+                          const void* w_uk, const float* w_uk_scale, __nv_bfloat16* q_full,
+                          cudaStream_t s);
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+cudaError_t launch_combine_uv(const DecodeArgs& a, WFmt wf, const void* w_uv,
+                              const float* w_uv_scale, __nv_bfloat16* out, float* lse_out,
+                              cudaStream_t s);
+
+}  // namespace mla

@@ -1,0 +1,114 @@
+"""CPU-side checks of the C ABI: the library loads, exports what the header declares,
+and rejects bad arguments before anything reaches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_decode_attention_06_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^(?:int|const char\*)\s+(mla_\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    for n in ("mla_decode_paged", "mla_decode_paged_fp8", "mla_decode_sparse",
+              "mla_decode_workspace_size", "mla_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    from mla_decode_attention_06_gb300 import _lib
+    for code in range(7):
+        assert _lib.status_string(code) != "unknown status"
+    assert _lib.status_string(99) == "unknown status"
+
+
+def _dims(**kw):
+    from mla_decode_attention_06_gb300 import MlaDims
+    d = dict(num_heads=128, qk_nope=128, qk_rope=64, kv_lora_rank=512, v_head=128, page_size=64,
+             num_pages=100)
+    d.update(kw)
+    return MlaDims(**d)
+
+
+def _opts(**kw):
+    from mla_decode_attention_06_gb300 import MlaOpts
+    o = dict(mask=1, window=0, scale=0.07, num_splits=4, flags=0)
+    o.update(kw)
+    return MlaOpts(**o)
+
+
+def test_workspace_size_grows_with_tokens_and_splits(lib):
+    n = ctypes.c_size_t()
+    assert lib.mla_decode_workspace_size(ctypes.byref(_dims()), ctypes.byref(_opts()), 64, 64,
+                                         ctypes.byref(n)) == 0
+    a = n.value
+    assert lib.mla_decode_workspace_size(ctypes.byref(_dims()), ctypes.byref(_opts()), 64, 128,
+                                         ctypes.byref(n)) == 0
+    assert n.value > a
+    assert lib.mla_decode_workspace_size(ctypes.byref(_dims()), ctypes.byref(_opts(num_splits=8)),
+                                         64, 64, ctypes.byref(n)) == 0
+    assert n.value > a
+    # q_full (128 rows x 576 bf16 per token) alone is 147456 bytes per token
+    assert a > 64 * 147456
+
+
+FAKE = 0x10000   # aligned, never dereferenced: every case below fails validation first
+
+
+def _paged(lib, dims=None, opts=None, q=FAKE, ws_bytes=1 << 40, bt_stride=4):
+    return lib.mla_decode_paged(ctypes.byref(dims or _dims()), ctypes.byref(opts or _opts()), q,
+                                FAKE, 2, 2, FAKE, FAKE, bt_stride, FAKE, FAKE, FAKE, FAKE, None,
+                                FAKE, ws_bytes, None)
+
+
+def test_invalid_arguments_are_rejected(lib):
+    assert _paged(lib, q=None) == 1                                   # NULL q
+    assert _paged(lib, q=FAKE + 2) == 1                               # misaligned q
+    assert _paged(lib, dims=_dims(num_heads=0)) == 1
+    assert _paged(lib, bt_stride=0) == 1
+    assert _paged(lib, opts=_opts(mask=7)) == 1
+    assert _paged(lib, opts=_opts(mask=2, window=0)) == 1             # SWC needs window >= 1
+    assert _paged(lib, opts=_opts(scale=float("nan"))) == 1
+    assert _paged(lib, opts=_opts(num_splits=-1)) == 1
+    assert _paged(lib, opts=_opts(flags=8)) == 1
+
+
+def test_unsupported_shapes_are_reported(lib):
+    assert _paged(lib, dims=_dims(num_heads=129)) == 2
+    assert _paged(lib, dims=_dims(kv_lora_rank=520)) == 2
+
+
+def test_workspace_too_small(lib):
+    assert _paged(lib, ws_bytes=1024) == 3
+
+
+def test_fp8_q_scale_and_sparse_mask_are_unsupported(lib):
+    rc = lib.mla_decode_paged_fp8(ctypes.byref(_dims()), ctypes.byref(_opts()), FAKE, FAKE, 2, 2,
+                                  FAKE, FAKE, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  None, FAKE, 1 << 40, None)
+    assert rc == 2
+    rc = lib.mla_decode_sparse(ctypes.byref(_dims()), ctypes.byref(_opts(mask=1)), FAKE, FAKE, 2,
+                               2, FAKE, FAKE, 16, None, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None)
+    assert rc == 2
