@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA decode µs/layer, HBM GB/s and tensor TFLOP/s vs roofline (B=64,H=128,4k)"
 UNIT = "us/layer"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+LAUNCHES_PER_CALL = 3       # absorb (+ plan), decode (+ split merge), W_uv
 CPU_SAMPLE_TOKENS = 48      # oracle sample for the CPU baseline (a few seconds of wall time)
 REF_SAMPLE_TOKENS = 2       # oracle sample per step of the reference arm
 KERNEL_SOURCES = {"decode_splitkv": "mla_decode_attention_06_gb300/csrc/mla_decode_simt.cu"}
@@ -51,11 +52,16 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="a smaller dsv3 case for ncu captures: batch 32 over an 8192-page pool "
+                         "(170 MB of attended cache, above the L2 size)")
     return ap.parse_args()
 
 
-def make_workload(name):
+def make_workload(name, profile_case=False):
     from workloads import mla as W
+    if profile_case:
+        return W.config_dsv3(B=32, num_pages=8192)
     return {"dsv3": W.config_dsv3, "long": W.config_long,
             "long_swc": lambda: W.config_long(window=4096), "fp8": W.config_fp8,
             "sparse": W.config_sparse}[name]()
@@ -171,6 +177,17 @@ class ClockSampler:
                 "samples": n}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The slowest rank's value (every rank calls this; identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -236,7 +253,7 @@ def main():
     import numpy as np
     import torch
 
-    p = make_workload(args.workload)
+    p = make_workload(args.workload, args.profile_case)
     if args.impl == "reference":
         run_reference(args, p)
         return
@@ -261,9 +278,9 @@ def main():
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(timing=False):
+    def step(timing=False, on_stream=None):
         run_gpu(p, d, num_splits=args.num_splits, out=out, lse_out=lse, workspace=ws,
-                stream=stream, timing=timing)
+                stream=on_stream or stream, timing=timing)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -291,11 +308,7 @@ def main():
     clk = clocks.stop()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kt, ncalls = M.kernel_times()
-    ms = statistics.mean(per_step)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(per_step), dev)
 
     alg = algorithmic(p)
     peaks, peak_kind = load_peaks()
@@ -329,11 +342,12 @@ def main():
                      "peak_source": f"hbm_gbs of {peak_kind}",
                      "algorithmic_bytes_per_launch": alg["decode_bytes"]},
         "kernel_ms": {k: v for k, v in kt.items()}, "kernel_calls_timed": ncalls,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": LAUNCHES_PER_CALL * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
 
+    line["graph"] = graph_replay(step, flush, stream, args.steps)
     if not args.no_e2e:
         line["e2e"] = e2e(p, d, args, dev, out, lse, ws, flush, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -345,6 +359,30 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def graph_replay(step, flush, stream, steps):
+    """The same call captured once in a CUDA graph and replayed (L2 flushed between replays)."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(on_stream=torch.cuda.current_stream())
+        times = []
+        for i in range(steps + 3):
+            flush.zero_()
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            g.replay()
+            e.record(stream)
+            if i >= 3:
+                times.append((s, e))
+        torch.cuda.synchronize()
+        us = statistics.mean(s.elapsed_time(e) for s, e in times) * 1e3
+        return {"us_per_call": us, "replays": len(times)}
+    except Exception as ex:   # capture is best effort; the eager number above is the metric
+        return {"error": str(ex)[:200]}
 
 
 def e2e(p, d, args, dev, out, lse, ws, flush, stream, world):
@@ -375,12 +413,7 @@ def e2e(p, d, args, dev, out, lse, ws, flush, stream, world):
         e.synchronize()
         if i >= 3:
             times.append(s.elapsed_time(e))
-    ms = statistics.mean(times)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(times), dev)
     return {"value": ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n}
 

@@ -55,7 +55,9 @@ extern "C" {
 typedef enum {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1,        /* NULL required pointer, bad sizes, bad mask or window */
-  MLA_ERR_UNSUPPORTED = 2,        /* shape without a kernel instance, H > 128, q_scale != NULL */
+  MLA_ERR_UNSUPPORTED = 2,        /* shape without a kernel instance, H > 128, q_scale != NULL;
+                                     instances: (L, R) = (512, 64), or L = 64 with R <= 32 (R % 8 == 0);
+                                     page_size in {8, 16, 32, 64} or a multiple of 64 */
   MLA_ERR_WORKSPACE_TOO_SMALL = 3,
   MLA_ERR_CUDA = 4,               /* a CUDA runtime or driver call failed */
   MLA_ERR_DEVICE_CHECK = 5,       /* debug mode: a device-side input check failed */
@@ -156,9 +158,10 @@ int mla_decode_sparse(const mla_dims_t* dims, const mla_opts_t* opts, const void
 
 /* Mean per-kernel device durations (milliseconds) over the calls on the current
  * device that set MLA_FLAG_KERNEL_TIMING since the previous read (at most the
- * last 4096), in launch order: [0] plan, [1] W_uk absorb, [2] split-KV decode,
- * [3] combine + W_uv.  Waits for those calls' events and clears the record.
- * Writes min(n, 4) values; returns the number of calls averaged, 0 if none,
+ * last 4096), in launch order: [0] W_uk absorb (with the call's planning),
+ * [1] split-KV decode (with the merge of split tokens), [2] W_uv.  Waits for
+ * those calls' events and clears the record.  Writes min(n, 3) values;
+ * returns the number of calls averaged, 0 if none,
  * -1 on a CUDA error.  Host-side bookkeeping only: not thread-safe. */
 int mla_decode_kernel_times(float* ms, int32_t n);
 

@@ -23,7 +23,7 @@ MLA_MASK_CAUSAL = 1
 MLA_MASK_SLIDING_WINDOW_CAUSAL = 2
 MLA_FLAG_DEBUG_CHECKS = 1
 MLA_FLAG_KERNEL_TIMING = 2
-KERNEL_NAMES = ("plan", "absorb_w_uk", "decode_splitkv", "combine_w_uv")
+KERNEL_NAMES = ("absorb_w_uk", "decode_splitkv", "w_uv")
 
 EXPORTED = ("mla_decode_workspace_size", "mla_decode_paged", "mla_decode_paged_fp8",
             "mla_decode_sparse", "mla_decode_kernel_times", "mla_status_string")
@@ -93,8 +93,8 @@ class MlaError(RuntimeError):
 def kernel_times():
     """Mean per-kernel durations (ms) over the calls made with MLA_FLAG_KERNEL_TIMING since
     the previous read, and the number of calls they average."""
-    buf = (ctypes.c_float * 4)()
-    n = load().mla_decode_kernel_times(buf, 4)
+    buf = (ctypes.c_float * len(KERNEL_NAMES))()
+    n = load().mla_decode_kernel_times(buf, len(KERNEL_NAMES))
     if n < 0:
         raise RuntimeError("mla_decode_kernel_times failed")
     return (dict(zip(KERNEL_NAMES, list(buf))) if n > 0 else {}), n

@@ -1,18 +1,19 @@
 // C ABI of libmla_decode.so: argument checks, workspace carving and the launch
-// sequence  K0 plan -> K1 absorb -> K2 split-KV decode -> K3 combine + W_uv.
+// sequence  K1 W_uk absorb (+ plan) -> K2 split-KV decode (+ split merge) -> K3 W_uv.
 // Nothing here allocates or synchronises unless MLA_FLAG_DEBUG_CHECKS is set.
 #include <cstdio>
 #include <cstring>
 #include <new>
 
 #include "mla_kernels.cuh"
+#include "mla_plan.cuh"
 
 using namespace mla;
 
 namespace {
 
 constexpr int kMaxSplits = 1 << 16;
-constexpr int kTimedKernels = 4;
+constexpr int kTimedKernels = 3;
 constexpr int kMaxDevices = 64;
 
 // Event sets of the timed calls made since the last read, per device
@@ -61,6 +62,7 @@ int check_dims(const mla_dims_t* d) {
   if (d->kv_lora_rank % 16 != 0 || d->kv_lora_rank > 512 || d->qk_rope % 2 != 0 || d->qk_nope % 2 != 0)
     return MLA_ERR_UNSUPPORTED;
   if ((int64_t)d->num_pages * d->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (!decode_tc_supported(*d)) return MLA_ERR_UNSUPPORTED;
   return MLA_OK;
 }
 
@@ -143,6 +145,21 @@ int run(const CallCommon& c) {
   a.lse_ws = reinterpret_cast<float*>(ws + lay.lse);
   a.part_o = reinterpret_cast<float*>(ws + lay.part_o);
   a.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
+  a.counters = reinterpret_cast<int*>(ws + lay.counters);
+  PlanInputs pin{};
+  pin.offsets = c.offsets;
+  pin.B = c.B;
+  pin.T = c.T;
+  pin.ks = c.ks;
+  pin.mask = c.o->mask;
+  pin.window = c.o->window;
+  pin.plan = plan;
+  pin.hdr = hdr;
+  pin.counters = a.counters;
+  pin.o_lat = a.o_lat;
+  pin.lse_ws = a.lse_ws;
+  pin.H = c.d->num_heads;
+  pin.L = c.d->kv_lora_rank;
 
   EventSet* timer = nullptr;
   if (c.o->flags & MLA_FLAG_KERNEL_TIMING) {
@@ -152,19 +169,19 @@ int run(const CallCommon& c) {
   auto mark = [&](int i) {
     return timer ? cudaEventRecord(timer->ev[i], c.stream) : cudaSuccess;
   };
+  // K1 absorb (+ plan) -> K2 split-KV decode (+ merge of split tokens) -> K3 W_uv;
+  // K2 and K3 are launched as programmatic dependents of their predecessor.
   cudaError_t e = mark(0);
-  if (e == cudaSuccess) e = launch_plan(c.offsets, c.B, c.T, c.ks, c.o->mask, c.o->window, plan, hdr, c.stream);
+  if (e == cudaSuccess)
+    e = launch_absorb_tc(*c.d, c.T, static_cast<const __nv_bfloat16*>(c.q), c.w_fmt, c.w_uk, c.w_uk_scale,
+                         reinterpret_cast<__nv_bfloat16*>(ws + lay.q_full), hdr, pin, c.stream);
   if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess)
-    e = launch_absorb(*c.d, c.T, static_cast<const __nv_bfloat16*>(c.q), c.w_fmt, c.w_uk, c.w_uk_scale,
-                      reinterpret_cast<__nv_bfloat16*>(ws + lay.q_full), c.stream);
+  if (e == cudaSuccess && c.T > 0) e = launch_decode_tc(a, c.stream);
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess && c.T > 0) e = launch_decode(a, c.stream);
-  if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
-    e = launch_combine_uv(a, c.w_fmt, c.w_uv, c.w_uv_scale, static_cast<__nv_bfloat16*>(c.out), c.lse_out,
-                          c.stream);
-  if (e == cudaSuccess) e = mark(4);
+    e = launch_uv_tc(*c.d, c.T, a.o_lat, c.w_fmt, c.w_uv, c.w_uv_scale, a.lse_ws, static_cast<__nv_bfloat16*>(c.out),
+                     c.lse_out, hdr, c.stream);
+  if (e == cudaSuccess) e = mark(3);
   if (e != cudaSuccess) {
     std::fprintf(stderr, "mla_decode: %s\n", cudaGetErrorString(e));
     return MLA_ERR_CUDA;
@@ -295,7 +312,7 @@ int mla_decode_kernel_times(float* ms, int32_t n) {
   const int calls = t.used;
   t.used = 0;
   if (calls == 0) return 0;
-  double sum[kTimedKernels] = {0, 0, 0, 0};
+  double sum[kTimedKernels] = {};
   for (int c = 0; c < calls; ++c) {
     const int slot = (t.next - 1 - c + 2 * kMaxTimedCalls) % kMaxTimedCalls;
     EventSet& es = t.sets[slot];

@@ -47,9 +47,17 @@ struct KeySource {
   int32_t num_pages;
 };
 
-// Byte offsets of the workspace sections.
+// Byte offsets of the workspace sections:
+//   header     PlanHeader (total tiles, status word)
+//   plan       TokenPlan [T]
+//   counters   int [T, 2]: partitions that finished a split token, per cluster rank
+//   q_full     bf16 [T, 128, L+R]: absorbed queries, rows h >= H zero
+//   o_lat      bf16 [T, H, L]: normalised latent outputs
+//   lse        fp32 [T, H]
+//   part_o     fp32 [K, 2, H, L]: partials of the first / last segment of each partition
+//   part_lse   fp32 [K, 2, 2, H]: their log-sum-exp, one copy per cluster rank
 struct WorkspaceLayout {
-  size_t header, plan, q_full, o_lat, lse, part_o, part_lse, total;
+  size_t header, plan, counters, q_full, o_lat, lse, part_o, part_lse, total;
 };
 
 // Host-side: the layout for T tokens and K KV partitions.
@@ -59,11 +67,12 @@ inline WorkspaceLayout workspace_layout(const mla_dims_t& d, int T, int K) {
   size_t o = 0;
   w.header = o;  o = up(o + sizeof(PlanHeader));
   w.plan = o;    o = up(o + sizeof(TokenPlan) * (size_t)(T > 0 ? T : 1));
+  w.counters = o; o = up(o + sizeof(int) * 2 * (size_t)(T > 0 ? T : 1));
   w.q_full = o;  o = up(o + (size_t)T * kMaxHeads * (d.kv_lora_rank + d.qk_rope) * 2);
   w.o_lat = o;   o = up(o + (size_t)T * d.num_heads * d.kv_lora_rank * 2);
   w.lse = o;     o = up(o + (size_t)T * d.num_heads * 4);
   w.part_o = o;  o = up(o + (size_t)K * 2 * d.num_heads * d.kv_lora_rank * 4);
-  w.part_lse = o; o = up(o + (size_t)K * 2 * d.num_heads * 4);
+  w.part_lse = o; o = up(o + (size_t)K * 2 * 2 * d.num_heads * 4);   // [K, slot, cta rank, H]
   w.total = o;
   return w;
 }

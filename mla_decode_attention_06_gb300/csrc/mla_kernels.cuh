@@ -24,20 +24,27 @@ struct DecodeArgs {
   __nv_bfloat16* o_lat;         // [T, H, L]
   float* lse_ws;                // [T, H]
   float* part_o;                // [K, 2, H, L]
-  float* part_lse;              // [K, 2, H]
+  float* part_lse;              // [K, 2, 2, H]
+  int* counters;                // [T, 2]
 };
 
-cudaError_t launch_plan(const uint32_t* offsets, int B, int T, const KeySource& ks, int mask,
-                        int window, TokenPlan* plan, PlanHeader* hdr, cudaStream_t s);
 
-cudaError_t launch_absorb(const mla_dims_t& d, int T, const __nv_bfloat16* q, WFmt wf,
-                          const void* w_uk, const float* w_uk_scale, __nv_bfloat16* q_full,
-                          cudaStream_t s);
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
-cudaError_t launch_combine_uv(const DecodeArgs& a, WFmt wf, const void* w_uv,
-                              const float* w_uv_scale, __nv_bfloat16* out, float* lse_out,
-                              cudaStream_t s);
+// Tensor-core decode (tcgen05): dense bf16 paged cache, shapes listed in decode_tc_supported.
+bool decode_tc_supported(const mla_dims_t& d);
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
+
+// Tensor-core weight GEMMs (K1 absorb, K3 W_uv) and the split-KV combine.
+// K1: the W_uk absorb; one of its blocks also runs the plan (PlanInputs).
+struct PlanInputs;
+cudaError_t launch_absorb_tc(const mla_dims_t& d, int T, const __nv_bfloat16* q, WFmt wf, const void* w_uk,
+                             const float* w_uk_scale, __nv_bfloat16* q_full, PlanHeader* hdr,
+                             const PlanInputs& plan, cudaStream_t s);
+cudaError_t launch_uv_tc(const mla_dims_t& d, int T, const __nv_bfloat16* o_lat, WFmt wf, const void* w_uv,
+                         const float* w_uv_scale, const float* lse_ws, __nv_bfloat16* out, float* lse_out,
+                         PlanHeader* hdr, cudaStream_t s);
+
+
 
 }  // namespace mla

@@ -1,0 +1,113 @@
+// Per-token key ranges and the global 64-key tile numbering that the decode's
+// KV partitions split evenly (the on-device counterpart of the packed dispatch
+// metadata `scalar_args_buf` and of `num_partitions_in` on the
+// generic_flare_mla_decode_kv_cache_ragged page).  Run by one thread block
+// inside the first kernel of a call.
+#pragma once
+#include <math_constants.h>
+
+#include "mla_common.cuh"
+
+namespace mla {
+
+struct PlanInputs {
+  const uint32_t* offsets;   // [B+1]
+  int B, T;
+  KeySource ks;
+  int mask, window;
+  TokenPlan* plan;           // [T]
+  PlanHeader* hdr;
+  int* counters;             // [T, 2] split-token arrival counters, zeroed here
+  __nv_bfloat16* o_lat;      // [T, H, L]: zeroed for tokens without keys
+  float* lse_ws;             // [T, H]:    -inf for tokens without keys
+  int H, L;
+};
+
+// Whole block (blockDim.x a multiple of 32, <= 1024).  Each thread owns a
+// contiguous run of tokens and counts their tiles; a block-wide exclusive scan
+// numbers the tiles globally.
+__device__ __forceinline__ void plan_block(const PlanInputs& in) {
+  __shared__ int warp_sums[32];
+  __shared__ int any_bad;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  if (tid == 0) {
+    any_bad = 0;
+    atomicExch(&in.hdr->status, 0);   // the plan runs first in every call
+  }
+  __syncthreads();
+  const int per = (in.T + nthr - 1) / nthr;
+  const int t0 = min(in.T, tid * per), t1 = min(in.T, t0 + per);
+  const KeySource& ks = in.ks;
+  int my_tiles = 0;
+  bool bad = false;
+  for (int t = t0; t < t1; ++t) {
+    int lo_b = 0, hi_b = in.B - 1;   // request of token t: last b with offsets[b] <= t
+    while (lo_b < hi_b) {
+      const int mid = (lo_b + hi_b + 1) >> 1;
+      if ((int)in.offsets[mid] <= t) lo_b = mid; else hi_b = mid - 1;
+    }
+    const int b = lo_b;
+    const int qb = (int)in.offsets[b], qe = (int)in.offsets[b + 1];
+    int lo = 0, hi = 0;
+    bool ok = qb <= t && t < qe && (int)in.offsets[in.B] == in.T;
+    if (ks.indices) {
+      int cnt = ks.topk_lengths ? ks.topk_lengths[b] : ks.idx_stride;
+      if (cnt < 0) { cnt = 0; ok = false; }
+      hi = min(cnt, ks.idx_stride);
+    } else {
+      const int len = (int)ks.cache_lens[b];
+      const int pos = len - (qe - qb) + (t - qb);
+      if (len > ks.bt_stride * ks.page_size || pos < 0) ok = false;
+      if (in.mask == MLA_MASK_NULL) { lo = 0; hi = len; }
+      else if (in.mask == MLA_MASK_CAUSAL) { lo = 0; hi = pos + 1; }
+      else { hi = pos + 1; lo = max(0, hi - in.window); }
+    }
+    if (!ok) { lo = 0; hi = 0; bad = true; }
+    TokenPlan p;
+    p.b = b;
+    p.lo = lo;
+    p.hi = hi;
+    p.tile_first = hi > lo ? lo / kTileKeys : 0;
+    p.ntiles = hi > lo ? (hi + kTileKeys - 1) / kTileKeys - p.tile_first : 0;
+    p.tile_start = my_tiles;   // local for now
+    p.pad[0] = p.pad[1] = 0;
+    in.plan[t] = p;
+    my_tiles += p.ntiles;
+  }
+  if (bad) any_bad = 1;
+
+  const int lane = tid & 31, wid = tid >> 5;
+  int incl = my_tiles;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int v = lane < (nthr >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    warp_sums[lane] = v;   // inclusive warp totals
+  }
+  __syncthreads();
+  const int base = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - my_tiles;
+  for (int t = t0; t < t1; ++t) in.plan[t].tile_start += base;
+  for (int i = tid; i < 2 * in.T; i += nthr) in.counters[i] = 0;
+  if (tid == nthr - 1) in.hdr->total_tiles = base + my_tiles;
+  __syncthreads();
+  // tokens with no key: zero latent output and lse = -inf (the decode never visits them)
+  for (int t = 0; t < in.T; ++t) {
+    if (in.plan[t].ntiles != 0) continue;
+    for (int i = tid; i < in.H * in.L; i += nthr)
+      in.o_lat[(size_t)t * in.H * in.L + i] = __float2bfloat16_rn(0.f);
+    for (int i = tid; i < in.H; i += nthr) in.lse_ws[(size_t)t * in.H + i] = -CUDART_INF_F;
+  }
+  if (tid == 0 && any_bad) atomicOr(&in.hdr->status, kDeviceCheckFailed);
+}
+
+}  // namespace mla

@@ -1,0 +1,367 @@
+// K1 and K3 on tcgen05: the two per-head weight GEMMs of the absorbed MLA
+// decode (mla_decode_branch_fp8 page: "q_nope_proj = q_nope_t @ w_uk" and
+// "output = raw_output_t @ w_uv"; w_uk [num_heads, kv_latent_dim,
+// qk_nope_head_dim], w_uv [num_heads, v_head_dim, kv_latent_dim]).
+//
+// Both have the shape  D[m, t] = sum_k W[h, m, k] * X[t, h, k]  per head h:
+//   absorb (K1): W = w_uk, m = latent column l, k = nope column, X = q
+//                -> written as bf16 into q_full[t, h, l]; CTAs of the first
+//                   m block also copy q_rope into q_full[t, h, L:L+R].
+//   W_uv   (K3): W = w_uv, m = v column, k = latent column, X = o_lat
+//                -> written as bf16 into out[t, h, v] (and lse copied out).
+// One CTA owns 128 rows m of one head and up to 128 tokens: M = 128 (weight
+// rows), N = tokens, K streamed in 64-column boxes through a 4-deep TMA ring.
+// The weights are read once per token tile, which is what bounds these
+// kernels (HBM): 16.8 MB per weight at the DeepSeek-V3 shapes.
+//
+// FP8 weights: e4m3 codes are widened to bf16 (exactly: every e4m3 value is a
+// bf16 value) in shared memory, and the 128 x 128 block scale is applied in
+// the epilogue; because the scale changes every 128 columns of k, each
+// 128-wide k block accumulates into its own TMEM columns and the epilogue sums
+// scale_b * D_b.
+#include "mla_kernels.cuh"
+#include "mla_plan.cuh"
+#include "sm100_ptx.cuh"
+
+namespace mla {
+namespace wg {
+
+using namespace sm100;
+
+constexpr int kThreads = 128;
+constexpr int kStages = 4;
+constexpr int kMaxTokens = 128;            // tokens per CTA (MMA N)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kABytes = 128 * 128;         // 128 rows x 64 bf16
+constexpr int kA8Bytes = 128 * 64;         // 128 rows x 64 e4m3
+
+struct Maps {
+  CUtensorMap w;   // bf16 [H*M rows, K cols] (128B swizzle) or e4m3 [H*M, K] (no swizzle)
+  CUtensorMap x;   // bf16 3-D {Kx cols, H, T} (128B swizzle)
+};
+
+struct Args {
+  int mode;            // 0 absorb, 1 W_uv
+  int H, T, M, K;      // heads, tokens, weight rows per head, contraction length
+  int TN;              // tokens per CTA (multiple of 16, <= 128)
+  const float* wscale; // e4m3 block scales [H, ceil(M/128), ceil(K/128)]
+  // absorb
+  __nv_bfloat16* q_full; int KQ, L, R, N; const __nv_bfloat16* q;
+  // W_uv
+  __nv_bfloat16* out; int V; const float* lse_ws; float* lse_out;
+  PlanHeader* hdr;
+  PlanInputs pin;      // absorb: block (0, 0, 0) also plans the call
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, PlanHeader* hdr) {
+  if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+  atomicOr(&hdr->status, kDeviceTimeout);
+  return false;
+}
+
+// e4m3 byte pair -> bf16x2 through the exact fp8 -> half conversion.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  const float2 f = __half22float2(__half2(h));
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f.x)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f.y)) << 16);
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constant__ Maps maps, const Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int TN = a.TN;
+  const int kBBytes = TN * 128;
+  uint8_t* sA = sm;                                  // kStages x [128 x 64] bf16
+  uint8_t* sB = sA + kStages * kABytes;              // kStages x [TN x 64] bf16
+  uint8_t* sA8 = sB + kStages * kBBytes;             // kStages x [128 x 64] e4m3 (fp8 only)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sA8 + (kFp8 ? kStages * kA8Bytes : 0));
+  uint64_t* empty = full + kStages;
+  uint64_t* done = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mb = blockIdx.x, h = blockIdx.y, t0 = blockIdx.z * TN;
+  const int m0 = mb * 128;
+  const int nkb = (a.K + 63) / 64;                 // 64-wide k boxes
+  const int nkb128 = kFp8 ? (a.K + 127) / 128 : 1; // accumulators
+  const int ncols_needed = nkb128 * TN;
+  const uint32_t tcols = ncols_needed <= 32 ? 32 : ncols_needed <= 64 ? 64 : ncols_needed <= 128 ? 128
+                         : ncols_needed <= 256 ? 256 : 512;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+    prefetch_tensormap(&maps.w);
+    prefetch_tensormap(&maps.x);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t stage_bytes = (kFp8 ? kA8Bytes : kABytes) + kBBytes;
+
+  auto load_w = [&](int kb) {
+    const int s = kb % kStages;
+    if (kFp8) tma_load_2d(sA8 + s * kA8Bytes, &maps.w, &full[s], kb * 64, h * a.M + m0);
+    else tma_load_2d(sA + s * kABytes, &maps.w, &full[s], kb * 64, h * a.M + m0);
+  };
+  auto load_x = [&](int kb) {
+    const int s = kb % kStages;
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+            smem_u32(sB + s * kBBytes)),
+        "l"(reinterpret_cast<uint64_t>(&maps.x)), "r"(smem_u32(&full[s])), "r"(kb * 64), "r"(h), "r"(t0)
+        : "memory");
+  };
+  auto load = [&](int kb) {
+    mbar_arrive_expect_tx(&full[kb % kStages], stage_bytes);
+    load_w(kb);
+    load_x(kb);
+  };
+  // weights do not depend on the previous kernel: start streaming them first
+  if (tid == 0)
+    for (int kb = 0; kb < nkb && kb < kStages; ++kb) {
+      mbar_arrive_expect_tx(&full[kb], stage_bytes);
+      load_w(kb);
+    }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // o_lat / lse of the decode (W_uv)
+  if (tid == 0)
+    for (int kb = 0; kb < nkb && kb < kStages; ++kb) load_x(kb);
+
+  const uint32_t idesc = idesc_bf16_f32(128, TN, false, false);
+  bool ok = true;
+  for (int kb = 0; kb < nkb; ++kb) {
+    const int s = kb % kStages;
+    // every thread waits; the CTA proceeds only if all saw the stage arrive
+    if (!__syncthreads_and(wait_bar(&full[s], (kb / kStages) & 1, a.hdr))) {
+      ok = false;
+      break;
+    }
+    if (kFp8) {
+      // widen row `tid` of the e4m3 box into the 128B-swizzled bf16 layout
+      const uint8_t* src = sA8 + s * kA8Bytes + tid * 64;
+      uint8_t* dst = sA + s * kABytes + tid * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src + ch * 8);
+        uint4 v;
+        v.x = e4m3x2_to_bf16x2((uint16_t)(raw.x & 0xffff));
+        v.y = e4m3x2_to_bf16x2((uint16_t)(raw.x >> 16));
+        v.z = e4m3x2_to_bf16x2((uint16_t)(raw.y & 0xffff));
+        v.w = e4m3x2_to_bf16x2((uint16_t)(raw.y >> 16));
+        *reinterpret_cast<uint4*>(dst + ((ch ^ (tid & 7)) * 16)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+    }
+    tc_fence_after();
+    bool issued_ok = true;
+    if (tid == 0) {
+      const int acc = kFp8 ? (kb >> 1) : 0;
+      const bool first_in_acc = kFp8 ? ((kb & 1) == 0) : (kb == 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t ad = smem_desc(smem_u32(sA + s * kABytes) + kk * 32, 16, 1024, kLayoutSw128);
+        const uint64_t bd = smem_desc(smem_u32(sB + s * kBBytes) + kk * 32, 16, 1024, kLayoutSw128);
+        mma_ss(tmem + acc * TN, ad, bd, idesc, (first_in_acc && kk == 0) ? 0u : 1u);
+      }
+      mma_commit(&empty[s]);
+      if (kb + kStages < nkb) {
+        // the stage is refilled once the MMAs above have read it
+        issued_ok = wait_bar(&empty[s], (kb / kStages) & 1, a.hdr);
+        if (issued_ok) load(kb + kStages);
+      }
+    }
+    if (!__syncthreads_and(issued_ok)) {
+      ok = false;
+      break;
+    }
+  }
+  if (tid == 0) mma_commit(done);
+  __syncwarp();
+  const bool fin = wait_bar(done, 0, a.hdr);
+  tc_fence_after();
+
+  // ------------------------------------------------------------------ epilogue
+  const int row = 32 * warp + lane;    // weight row within the block = TMEM lane
+  const int m = m0 + row;
+  const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  float sc[4] = {1.f, 1.f, 1.f, 1.f};
+  if (kFp8) {
+    const int nmb = (a.M + 127) / 128;
+    for (int b = 0; b < nkb128 && b < 4; ++b) sc[b] = a.wscale[((size_t)h * nmb + mb) * nkb128 + b];
+  }
+  for (int j0 = 0; j0 < TN; j0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    for (int b = 0; b < nkb128; ++b) {
+      uint32_t r[16];
+      tmem_ld16(trow + b * TN + j0, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += sc[b] * __uint_as_float(r[i]);
+    }
+    if (!fin || !ok || m >= a.M) continue;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = t0 + j0 + i;
+      if (t >= a.T) break;
+      if (a.mode == 0)
+        a.q_full[((size_t)t * kMaxHeads + h) * a.KQ + m] = __float2bfloat16_rn(v[i]);
+      else
+        a.out[((size_t)t * a.H + h) * a.V + m] = __float2bfloat16_rn(v[i]);
+    }
+  }
+  if (mb == 0) {
+    if (a.mode == 0) {
+      // rope columns are copied unchanged; absent heads are zero rows
+      for (int i = tid; i < TN * a.R; i += kThreads) {
+        const int t = t0 + i / a.R, r = i % a.R;
+        if (t < a.T)
+          a.q_full[((size_t)t * kMaxHeads + h) * a.KQ + a.L + r] = a.q[((size_t)t * a.H + h) * (a.N + a.R) + a.N + r];
+      }
+      if (h == 0 && a.H < kMaxHeads) {
+        const int per = (kMaxHeads - a.H) * a.KQ;
+        for (int i = tid; i < TN * per; i += kThreads) {
+          const int t = t0 + i / per;
+          if (t < a.T) a.q_full[((size_t)t * kMaxHeads + a.H) * a.KQ + i % per] = __float2bfloat16_rn(0.f);
+        }
+      }
+    } else if (a.lse_out) {
+      for (int j = tid; j < TN; j += kThreads)
+        if (t0 + j < a.T) a.lse_out[(size_t)(t0 + j) * a.H + h] = a.lse_ws[(size_t)(t0 + j) * a.H + h];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tcols);
+  }
+  if (a.mode == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) plan_block(a.pin);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+cudaError_t launch(const Args& a0, WFmt wf, const void* w, const void* x, int Kx, cudaStream_t s) {
+  Args a = a0;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || a.T == 0) return a.T == 0 ? cudaSuccess : cudaErrorInvalidValue;
+  a.TN = a.T >= kMaxTokens ? kMaxTokens : ((a.T + 15) / 16) * 16;
+  Maps maps;
+  {
+    const bool f8 = wf == WFmt::kE4M3;
+    cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.H * a.M};
+    cuuint64_t strides[1] = {(cuuint64_t)a.K * (f8 ? 1 : 2)};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    if (fn(&maps.w, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w),
+           dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           f8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)Kx, (cuuint64_t)a.H, (cuuint64_t)a.T};
+    cuuint64_t strides[2] = {(cuuint64_t)Kx * 2, (cuuint64_t)a.H * Kx * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)a.TN};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (fn(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const bool f8 = wf == WFmt::kE4M3;
+  const size_t smem = 1024 + kStages * (kABytes + a.TN * 128) + (f8 ? kStages * kA8Bytes : 0) + 256;
+  dim3 grid((a.M + 127) / 128, a.H, (a.T + a.TN - 1) / a.TN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // W_uv overlaps the decode's tail
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.mode == 1 ? 1 : 0;
+  cudaError_t e;
+  if (f8) {
+    e = cudaFuncSetAttribute(wgemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, wgemm_kernel<true>, maps, a);
+  } else {
+    e = cudaFuncSetAttribute(wgemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, wgemm_kernel<false>, maps, a);
+  }
+  return e;
+}
+
+}  // namespace wg
+
+cudaError_t launch_absorb_tc(const mla_dims_t& d, int T, const __nv_bfloat16* q, WFmt wf, const void* w_uk,
+                             const float* w_uk_scale, __nv_bfloat16* q_full, PlanHeader* hdr,
+                             const PlanInputs& plan, cudaStream_t s) {
+  wg::Args a{};
+  a.mode = 0;
+  a.H = d.num_heads;
+  a.T = T;
+  a.M = d.kv_lora_rank;
+  a.K = d.qk_nope;
+  a.wscale = w_uk_scale;
+  a.q_full = q_full;
+  a.KQ = d.kv_lora_rank + d.qk_rope;
+  a.L = d.kv_lora_rank;
+  a.R = d.qk_rope;
+  a.N = d.qk_nope;
+  a.q = q;
+  a.hdr = hdr;
+  a.pin = plan;
+  return wg::launch(a, wf, w_uk, q, d.qk_nope + d.qk_rope, s);
+}
+
+cudaError_t launch_uv_tc(const mla_dims_t& d, int T, const __nv_bfloat16* o_lat, WFmt wf, const void* w_uv,
+                         const float* w_uv_scale, const float* lse_ws, __nv_bfloat16* out, float* lse_out,
+                         PlanHeader* hdr, cudaStream_t s) {
+  wg::Args a{};
+  a.mode = 1;
+  a.H = d.num_heads;
+  a.T = T;
+  a.M = d.v_head;
+  a.K = d.kv_lora_rank;
+  a.wscale = w_uv_scale;
+  a.out = out;
+  a.V = d.v_head;
+  a.lse_ws = lse_ws;
+  a.lse_out = lse_out;
+  a.hdr = hdr;
+  return wg::launch(a, wf, w_uv, o_lat, d.kv_lora_rank, s);
+}
+
+}  // namespace mla

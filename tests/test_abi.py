@@ -21,7 +21,7 @@ def declared_functions():
     for fn in os.listdir(os.path.join(ROOT, "include")):
         if fn.endswith(".h"):
             src = open(os.path.join(ROOT, "include", fn)).read()
-            names += re.findall(r"^(?:int|const char\*)\s+(mla_\w+)\s*\(", src, flags=re.M)
+            names += re.findall(r"^(?:int|size_t|const char\*)\s+(mla_\w+)\s*\(", src, flags=re.M)
     return names
 
 
@@ -98,6 +98,8 @@ def test_invalid_arguments_are_rejected(lib):
 def test_unsupported_shapes_are_reported(lib):
     assert _paged(lib, dims=_dims(num_heads=129)) == 2
     assert _paged(lib, dims=_dims(kv_lora_rank=520)) == 2
+    assert _paged(lib, dims=_dims(kv_lora_rank=256)) == 2          # no tensor-core instance
+    assert _paged(lib, dims=_dims(page_size=48)) == 2              # pages must tile 64-key tiles
 
 
 def test_workspace_too_small(lib):

@@ -373,10 +373,10 @@ def config_tiny(seed: int = 1000) -> MlaProblem:
                       num_pages=8, mask=MASK_CAUSAL)
 
 
-def config_dsv3(seed: int = 1001, B: int = 64) -> MlaProblem:
+def config_dsv3(seed: int = 1001, B: int = 64, num_pages: int = 40000) -> MlaProblem:
     """B=64, H=128, lens U[1024, 8192], 64-token pages over a 40k-page pool, RMS-normalised c_kv."""
     lens = Stream(seed, "dsv3-lens").integers(1024, 8192, B)
-    return make_dense("dsv3_bf16", seed, **DSV3, ps=64, cache_lens=lens, num_pages=40000,
+    return make_dense("dsv3_bf16", seed, **DSV3, ps=64, cache_lens=lens, num_pages=num_pages,
                       mask=MASK_CAUSAL, rms_norm=True)
 
 
