@@ -187,11 +187,18 @@ int run(const CallCommon& c) {
     return MLA_ERR_CUDA;
   }
   if (c.o->flags & MLA_FLAG_DEBUG_CHECKS) {
-    int status = 0;
-    if (cudaMemcpyAsync(&status, &hdr->status, sizeof(int), cudaMemcpyDeviceToHost, c.stream) != cudaSuccess ||
+    int st_words[4] = {0, 0, 0, 0};   // status, total tiles unused, time-out record
+    if (cudaMemcpyAsync(st_words, &hdr->status, sizeof(int), cudaMemcpyDeviceToHost, c.stream) != cudaSuccess ||
+        cudaMemcpyAsync(st_words + 2, &hdr->pad[0], 2 * sizeof(int), cudaMemcpyDeviceToHost, c.stream) !=
+            cudaSuccess ||
         cudaStreamSynchronize(c.stream) != cudaSuccess)
       return MLA_ERR_CUDA;
-    if (status & kDeviceTimeout) return MLA_ERR_TIMEOUT;
+    const int status = st_words[0];
+    if (status & kDeviceTimeout) {
+      std::fprintf(stderr, "mla_decode: device wait timed out (barrier smem offset 0x%x, thread %d, block %d)\n",
+                   st_words[2] & 0x3FFFF, (st_words[2] >> 18) & 0x1FFF, st_words[3]);
+      return MLA_ERR_TIMEOUT;
+    }
     if (status & kDeviceCheckFailed) return MLA_ERR_DEVICE_CHECK;
   }
   return MLA_OK;

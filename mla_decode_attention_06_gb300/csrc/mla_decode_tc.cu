@@ -81,6 +81,7 @@ struct Smem {   // control block at the end of dynamic shared memory
   uint64_t kv_conv[kStages];     // e4m3 rows widened (kLoadFp8)
   uint64_t conv_sync;            // converters: every row read before any is overwritten
   uint64_t fix_bar, fix_done;    // softmax: partial written / merge decision published
+  uint64_t bye;                  // the peer CTA is done touching this CTA's shared memory
   uint64_t row_mask[kStages];
   int32_t rowid[kStages][64];    // physical row of each tile row (kLoadFp8, kLoadSparse)
   uint32_t tmem_base;
@@ -101,9 +102,17 @@ __device__ __forceinline__ void for_each_segment(const DecodeArgs& a, int g0, in
   int si = 0;
   while (g < g1) {
     const int t = token_of_tile(a.plan, a.T, g);
+    if (t < 0 || t >= a.T) {   // a plan that does not cover g: report, never loop
+      atomicOr(&a.hdr_mut->status, kDeviceCheckFailed);
+      return;
+    }
     const TokenPlan tp = a.plan[t];
     const int ia = g - tp.tile_start;
     const int ie = min(g1, tp.tile_start + tp.ntiles) - tp.tile_start;
+    if (ia < 0 || ie <= ia) {
+      atomicOr(&a.hdr_mut->status, kDeviceCheckFailed);
+      return;
+    }
     f(si, t, tp, ia, ie, g == g0);
     g = tp.tile_start + ie;
     ++si;
@@ -114,8 +123,15 @@ __device__ __forceinline__ bool aborted(const Smem* cs) {
   return *reinterpret_cast<const volatile int*>(&cs->abort) != 0;
 }
 
+// First time-out of a call: barrier offset in shared memory, thread and block.
+__device__ __forceinline__ void record_timeout(uint64_t* bar, PlanHeader* hdr) {
+  const int code = (int)(0x80000000u | ((uint32_t)threadIdx.x << 18) | (smem_u32(bar) & 0x3FFFFu));
+  if (atomicCAS(&hdr->pad[0], 0, code) == 0) hdr->pad[1] = (int)blockIdx.x;
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Smem* cs, PlanHeader* hdr) {
   if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+  record_timeout(bar, hdr);
   atomicOr(&hdr->status, kDeviceTimeout);
   *reinterpret_cast<volatile int*>(&cs->abort) = 1;
   return false;
@@ -124,6 +140,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
 __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t parity, Smem* cs,
                                                       PlanHeader* hdr) {
   if (mbar_wait<true>(bar, parity, kWaitLimitNs)) return true;
+  record_timeout(bar, hdr);
   atomicOr(&hdr->status, kDeviceTimeout);
   *reinterpret_cast<volatile int*>(&cs->abort) = 1;
   return false;
@@ -197,6 +214,18 @@ __device__ __noinline__ void merge_split_token(const DecodeArgs& a, int t, const
   if (rank == 0) a.lse_ws[(size_t)t * H + row] = mx != -CUDART_INF_F ? mx + __logf(sum) : -CUDART_INF_F;
 }
 
+// Warp-uniform forms: every lane waits, then the warp votes, so lanes never
+// diverge around warp-collective instructions (tcgen05.ld/st, shuffles, votes).
+__device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, Smem* cs, PlanHeader* hdr) {
+  const bool ok = wait_or_abort(bar, parity, cs, hdr);
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool wwait_cluster(uint64_t* bar, uint32_t parity, Smem* cs, PlanHeader* hdr) {
+  const bool ok = wait_cluster_or_abort(bar, parity, cs, hdr);
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool waborted(const Smem* cs) { return __any_sync(0xffffffffu, aborted(cs)); }
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -244,6 +273,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     mbar_init(&cs->conv_sync, 64);
     mbar_init(&cs->fix_bar, 128);
     mbar_init(&cs->fix_done, 1);
+    mbar_init(&cs->bye, 1);
     cs->abort = 0;
     fence_mbar_init();
   }
@@ -276,8 +306,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     int c = 0;
     bool bad = false;
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
-      if (aborted(cs)) return;
-      if (si > 0 && !wait_or_abort(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
+      if (waborted(cs)) return;
+      if (si > 0 && !wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
       if (lane == 0) {
         mbar_arrive_expect_tx(&cs->q_full, C::kQBytes);
         for (int i = 0; i < C::NLB; ++i)
@@ -285,9 +315,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         tma_load_2d(sQ + C::NLB * C::kLatBoxQ, &maps.q_rope, &cs->q_full, rope_x0, t * kMaxHeads);
       }
       for (int it = ia; it < ie; ++it, ++c) {
-        if (aborted(cs)) return;
+        if (waborted(cs)) return;
         const int s = c % kStages;
-        if (c >= kStages && !wait_or_abort(&cs->kv_empty[s], ((c / kStages) & 1) ^ 1, cs, hdr)) return;
+        if (c >= kStages && !wwait(&cs->kv_empty[s], ((c / kStages) & 1) ^ 1, cs, hdr)) return;
         const int key0 = (tp.tile_first + it) * kTileKeys;
         // rows j and j + 32 of this tile: which key / slot, and is it live?
         bool v[2];
@@ -385,8 +415,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     int seg_of_prev = -1;
     auto issue_pv = [&](int si) {
       // P(prev) is in TMEM, O is free for the segment's first PV
-      if (!wait_or_abort(&cs->p_full[prev_b], (prev_c / 2) & 1, cs, hdr)) return false;
-      if (first_pv_of_seg && si > 0 && !wait_or_abort(&cs->o_free, (si - 1) & 1, cs, hdr)) return false;
+      if (!wwait(&cs->p_full[prev_b], (prev_c / 2) & 1, cs, hdr)) return false;
+      if (first_pv_of_seg && si > 0 && !wwait(&cs->o_free, (si - 1) & 1, cs, hdr)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t st = sSa + prev_s * C::kStageBytes;
@@ -404,15 +434,15 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       return true;
     };
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
-      if (aborted(cs)) return;
-      if (!wait_or_abort(&cs->q_full, si & 1, cs, hdr)) return;
+      if (waborted(cs)) return;
+      if (!wwait(&cs->q_full, si & 1, cs, hdr)) return;
       first_pv_of_seg = true;
       for (int it = ia; it < ie; ++it, ++c) {
-        if (aborted(cs)) return;
+        if (waborted(cs)) return;
         const int s = c % kStages, b = c & 1;
         if (MODE == kLoadFp8) {
-          if (!wait_or_abort(&cs->kv_conv[s], (c / kStages) & 1, cs, hdr)) return;
-        } else if (!wait_or_abort(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) {
+          if (!wwait(&cs->kv_conv[s], (c / kStages) & 1, cs, hdr)) return;
+        } else if (!wwait(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) {
           return;
         }
         const uint64_t mask = cs->row_mask[s];
@@ -471,9 +501,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     int c = 0;
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
       for (int it = ia; it < ie; ++it, ++c) {
-        if (aborted(cs)) return;
+        if (waborted(cs)) return;
         const int s = c % kStages;
-        if (!wait_or_abort(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) return;
+        if (!wwait(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) return;
         uint8_t* st = sStage + s * C::kStageBytes;
         const bool live = (cs->row_mask[s] >> ci) & 1ull;
         const float sc = live ? a.kv_scales[cs->rowid[s][ci]] : 0.f;
@@ -482,7 +512,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         for (int q = 0; q < LC / 16; ++q) raw[q] = *reinterpret_cast<const uint4*>(st + ci * LC + q * 16);
         // all rows are read before any is overwritten (the codes live where the bf16 rows go)
         mbar_arrive(&cs->conv_sync);
-        if (!wait_or_abort(&cs->conv_sync, c & 1, cs, hdr)) return;
+        if (!wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
 #pragma unroll
         for (int q = 0; q < LC / 16; ++q) {
           const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
@@ -522,15 +552,15 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     int c = 0;
     int nfix = 0;   // split-token merges attempted (phase of fix_bar / fix_done)
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg) {
-      if (aborted(cs)) return;
+      if (waborted(cs)) return;
       float m = -CUDART_INF_F, l = 0.f;
       int last_c = -1;
       for (int it = ia; it < ie; ++it, ++c) {
-        if (aborted(cs)) return;
+        if (waborted(cs)) return;
         const int s = c % kStages, b = c & 1;
-        if (!wait_or_abort(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) return;   // row mask visibility
+        if (!wwait(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) return;   // row mask visibility
         const uint64_t mask = cs->row_mask[s];
-        if (!wait_or_abort(&cs->s_full[b], (c >> 1) & 1, cs, hdr)) return;
+        if (!wwait(&cs->s_full[b], (c >> 1) & 1, cs, hdr)) return;
         tc_fence_after();
         float sv[64];
 #pragma unroll
@@ -543,7 +573,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         }
         if (CL == 2) {
           // my partial S -> peer's exchange buffer; peer's partial arrives in mine
-          if (c > 0 && !wait_cluster_or_abort(&cs->x_empty, (c - 1) & 1, cs, hdr)) return;
+          if (c > 0 && !wwait_cluster(&cs->x_empty, (c - 1) & 1, cs, hdr)) return;
 #pragma unroll
           for (int ch = 0; ch < 16; ++ch) {
             const int pos = ch ^ (row & 15);
@@ -552,7 +582,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
                           __float_as_uint(sv[4 * ch + 3]));
           }
           mbar_arrive_cluster(peer_xfull);
-          if (!wait_cluster_or_abort(&cs->x_full, c & 1, cs, hdr)) return;
+          if (!wwait_cluster(&cs->x_full, c & 1, cs, hdr)) return;
 #pragma unroll
           for (int ch = 0; ch < 16; ++ch) {
             const int pos = ch ^ (row & 15);
@@ -570,26 +600,31 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           sv[j] = ((mask >> j) & 1ull) ? sv[j] * sl2 : -CUDART_INF_F;
           mx = fmaxf(mx, sv[j]);
         }
-        if (mx > m + kRescaleThreshold || (m == -CUDART_INF_F && mx != -CUDART_INF_F)) {
-          if (m != -CUDART_INF_F) {
-            // O holds earlier tiles of this segment: scale it by 2^(m - mx) once PV(c-1) is done
-            const float alpha = ex2(m - mx);
-            if (!wait_or_abort(&cs->pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, cs, hdr)) return;
-            tc_fence_after();
+        // Lazy rescale: a row moves its reference max only when the new max is
+        // more than 2^8 above it.  tcgen05.ld/st are warp-collective, so when any
+        // row of the warp needs O rescaled the whole warp runs the loop (alpha = 1
+        // for the others).
+        const bool want = m != -CUDART_INF_F && mx > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, want)) {
+          const float alpha = want ? ex2(m - mx) : 1.f;
+          if (!wwait(&cs->pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, cs, hdr)) return;
+          tc_fence_after();
 #pragma unroll 1
-            for (int col = 0; col < LC; col += 16) {
-              uint32_t r[16];
-              tmem_ld16(trow + col, r);
-              tmem_ld_wait();
+          for (int col = 0; col < LC; col += 16) {
+            uint32_t r[16];
+            tmem_ld16(trow + col, r);
+            tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-              tmem_st16(trow + col, r);
-            }
-            tmem_st_wait();
-            l *= alpha;
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st16(trow + col, r);
           }
-          m = mx;
+          tmem_st_wait();
+          if (want) {
+            l *= alpha;
+            m = mx;
+          }
         }
+        if (m == -CUDART_INF_F) m = mx;   // first live key of the segment: O is still empty
         uint32_t pk[32];
         float psum = 0.f;
 #pragma unroll
@@ -618,7 +653,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       }
       if (last_c < 0) return;
       // ------------------------------------------------------------- epilogue
-      if (!wait_or_abort(&cs->pv_done[last_c & 1], (last_c >> 1) & 1, cs, hdr)) return;
+      if (!wwait(&cs->pv_done[last_c & 1], (last_c >> 1) & 1, cs, hdr)) return;
       tc_fence_after();
       const bool complete = ia == 0 && ie == tp.ntiles;
       const int slot = is_first_seg ? 0 : 1;
@@ -664,13 +699,17 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         mbar_arrive(&cs->fix_bar);
         const int Qt = (total + a.K - 1) / a.K;
         const int kf = tp.tile_start / Qt, kl = (tp.tile_start + tp.ntiles - 1) / Qt;
+        bool ok0 = true;
         if (row == 0) {
-          if (!wait_or_abort(&cs->fix_bar, nfix & 1, cs, hdr)) return;
-          const int prev = atomicAdd(&a.counters[2 * t + rank], 1);
-          cs->fix_last = prev == kl - kf;
-          mbar_arrive(&cs->fix_done);
+          ok0 = wait_or_abort(&cs->fix_bar, nfix & 1, cs, hdr);
+          if (ok0) {
+            const int prev = atomicAdd(&a.counters[2 * t + rank], 1);
+            cs->fix_last = prev == kl - kf;
+            mbar_arrive(&cs->fix_done);
+          }
         }
-        if (!wait_or_abort(&cs->fix_done, nfix & 1, cs, hdr)) return;
+        const bool ok1 = wait_or_abort(&cs->fix_done, nfix & 1, cs, hdr);
+        if (!__all_sync(0xffffffffu, ok0 && ok1)) return;
         ++nfix;
         if (cs->fix_last) {
           __threadfence();
@@ -683,7 +722,17 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
 
   // ------------------------------------------------------------- teardown
   tc_fence_before();
-  if (CL == 2) cluster_sync(); else __syncthreads();
+  __syncthreads();
+  if (CL == 2 && tid == 0) {
+    // every remote store / arrive of this CTA is issued; tell the peer, and wait
+    // (bounded) until the peer says the same before this CTA's memory goes away
+    mbar_arrive_cluster(mapa_shared(smem_u32(&cs->bye), peer));
+    if (!mbar_wait<true>(&cs->bye, 0, kWaitLimitNs)) {
+      record_timeout(&cs->bye, hdr);
+      atomicOr(&hdr->status, kDeviceTimeout);
+    }
+  }
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);

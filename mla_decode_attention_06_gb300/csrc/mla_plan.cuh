@@ -33,6 +33,8 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   if (tid == 0) {
     any_bad = 0;
     atomicExch(&in.hdr->status, 0);   // the plan runs first in every call
+    in.hdr->pad[0] = 0;               // time-out record
+    in.hdr->pad[1] = 0;
   }
   __syncthreads();
   const int per = (in.T + nthr - 1) / nthr;
