@@ -165,6 +165,30 @@ int mla_decode_sparse(const mla_dims_t* dims, const mla_opts_t* opts, const void
  * -1 on a CUDA error.  Host-side bookkeeping only: not thread-safe. */
 int mla_decode_kernel_times(float* ms, int32_t n);
 
+/* Dense bf16 decode for callers that cannot allocate device memory (code that
+ * runs where cudaMalloc is forbidden or unwanted: inside another allocator,
+ * under a memory budget fixed at start-up, or in a plug-in handed only its
+ * tensors).  No counterpart on the API pages: it is mla_decode_paged with the
+ * workspace replaced by a 64 MiB array compiled into the library
+ * (mla_decode_static_scratch_bytes() returns the size).  Arguments as
+ * mla_decode_paged without workspace / workspace_bytes.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - Each GPU on which this entry point's module is loaded keeps the 64 MiB
+ *     until the process exits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before capturing a stream into a CUDA graph.
+ *   - All calls share the one array: calls that may overlap on the GPU (other
+ *     streams, other host threads) race and must be serialised by the caller.
+ *   - Returns MLA_ERR_WORKSPACE_TOO_SMALL, with a message on stderr, when
+ *     mla_decode_workspace_size() for these arguments exceeds the array. */
+size_t mla_decode_static_scratch_bytes(void);
+int mla_decode_paged_static(const mla_dims_t* dims, const mla_opts_t* opts, const void* q,
+                            const uint32_t* input_row_offsets, int32_t batch, int32_t total_q,
+                            const void* kv_pool, const int32_t* block_table, int32_t block_table_stride,
+                            const uint32_t* cache_lens, const void* w_uk, const void* w_uv, void* out,
+                            float* lse_out, void* stream);
+
 /* Static text for a status code. */
 const char* mla_status_string(int status);
 
