@@ -251,7 +251,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   PlanHeader* hdr = a.hdr_mut;
   const int L = a.d.kv_lora_rank, H = a.d.num_heads;
   const int lat_x0 = (int)rank * LC;
-  // rope columns in element units of the map: the e4m3 pool's bf16 view starts rope at L/2
+  // this CTA's rope columns: in the absorbed query row they start at L; in the
+  // cache they start at L too, except in the e4m3 pool's bf16 view (L / 2)
+  const int q_rope_x0 = L + (int)rank * (a.d.qk_rope / CL);
   const int rope_x0 = (MODE == kLoadFp8 ? L / 2 : L) + (int)rank * (a.d.qk_rope / CL);
 
   if (tid == 0) {
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       mbar_init(&cs->pv_done[b], 1);
     }
     mbar_init(&cs->o_free, 128);
-    mbar_init(&cs->x_full, 128);
+    mbar_init(&cs->x_full, 1);   // expect_tx by row 0 + 32 KB of st.async from the peer
     mbar_init(&cs->x_empty, 128);
     mbar_init(&cs->conv_sync, 64);
     mbar_init(&cs->fix_bar, 128);
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         mbar_arrive_expect_tx(&cs->q_full, C::kQBytes);
         for (int i = 0; i < C::NLB; ++i)
           tma_load_2d(sQ + i * C::kLatBoxQ, &maps.q_lat, &cs->q_full, lat_x0 + 64 * i, t * kMaxHeads);
-        tma_load_2d(sQ + C::NLB * C::kLatBoxQ, &maps.q_rope, &cs->q_full, rope_x0, t * kMaxHeads);
+        tma_load_2d(sQ + C::NLB * C::kLatBoxQ, &maps.q_rope, &cs->q_full, q_rope_x0, t * kMaxHeads);
       }
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
@@ -562,31 +564,28 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         const uint64_t mask = cs->row_mask[s];
         if (!wwait(&cs->s_full[b], (c >> 1) & 1, cs, hdr)) return;
         tc_fence_after();
+        // S row (64 fp32) for this thread's head; both halves of the load in flight at once
+        uint32_t sr[64];
+        tmem_ld32(trow + C::kSCol + 64 * b, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(trow + C::kSCol + 64 * b + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld_wait();
         float sv[64];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          uint32_t r[16];
-          tmem_ld16(trow + C::kSCol + 64 * b + 16 * h, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) sv[16 * h + i] = __uint_as_float(r[i]);
-        }
+        for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(sr[j]);
         if (CL == 2) {
-          // my partial S -> peer's exchange buffer; peer's partial arrives in mine
+          // my partial S goes to the peer with asynchronous stores that count bytes on
+          // the peer's x_full; the peer's partial arrives in mine the same way
           if (c > 0 && !wwait_cluster(&cs->x_empty, (c - 1) & 1, cs, hdr)) return;
+          if (row == 0) mbar_arrive_expect_tx(&cs->x_full, 128 * 64 * 4);
+          const uint32_t dst = peer_x + (uint32_t)(row * 256);
 #pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            const int pos = ch ^ (row & 15);
-            st_cluster_v4(peer_x + (uint32_t)(row * 256 + pos * 16), __float_as_uint(sv[4 * ch]),
-                          __float_as_uint(sv[4 * ch + 1]), __float_as_uint(sv[4 * ch + 2]),
-                          __float_as_uint(sv[4 * ch + 3]));
-          }
-          mbar_arrive_cluster(peer_xfull);
+          for (int ch = 0; ch < 16; ++ch)
+            st_async_v4(dst + (uint32_t)((ch ^ (row & 15)) * 16), sr[4 * ch], sr[4 * ch + 1], sr[4 * ch + 2],
+                        sr[4 * ch + 3], peer_xfull);
           if (!wwait_cluster(&cs->x_full, c & 1, cs, hdr)) return;
 #pragma unroll
           for (int ch = 0; ch < 16; ++ch) {
-            const int pos = ch ^ (row & 15);
-            const float4 pv = *reinterpret_cast<const float4*>(sX + row * 64 + pos * 4);
+            const float4 pv = *reinterpret_cast<const float4*>(sX + row * 64 + (ch ^ (row & 15)) * 4);
             sv[4 * ch] += pv.x;
             sv[4 * ch + 1] += pv.y;
             sv[4 * ch + 2] += pv.z;
@@ -594,11 +593,19 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           }
           mbar_arrive_cluster(peer_xempty);
         }
-        float mx = -CUDART_INF_F;
+        // row max of the scaled scores (log2 domain); dead keys do not count
+        const bool all_live = mask == ~0ull;
+        float mx;
+        if (sl2 >= 0.f) {
+          float r = -CUDART_INF_F;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          sv[j] = ((mask >> j) & 1ull) ? sv[j] * sl2 : -CUDART_INF_F;
-          mx = fmaxf(mx, sv[j]);
+          for (int j = 0; j < 64; ++j) r = fmaxf(r, (all_live || ((mask >> j) & 1ull)) ? sv[j] : -CUDART_INF_F);
+          mx = r == -CUDART_INF_F ? r : r * sl2;
+        } else {
+          float r = CUDART_INF_F;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) r = fminf(r, (all_live || ((mask >> j) & 1ull)) ? sv[j] : CUDART_INF_F);
+          mx = r == CUDART_INF_F ? -CUDART_INF_F : r * sl2;
         }
         // Lazy rescale: a row moves its reference max only when the new max is
         // more than 2^8 above it.  tcgen05.ld/st are warp-collective, so when any
@@ -610,13 +617,13 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           if (!wwait(&cs->pv_done[(c - 1) & 1], ((c - 1) >> 1) & 1, cs, hdr)) return;
           tc_fence_after();
 #pragma unroll 1
-          for (int col = 0; col < LC; col += 16) {
-            uint32_t r[16];
-            tmem_ld16(trow + col, r);
+          for (int col = 0; col < LC; col += 32) {
+            uint32_t r[32];
+            tmem_ld32(trow + col, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st16(trow + col, r);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(trow + col, r);
           }
           tmem_st_wait();
           if (want) {
@@ -625,28 +632,24 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           }
         }
         if (m == -CUDART_INF_F) m = mx;   // first live key of the segment: O is still empty
+        // P = 2^(scale * log2(e) * s - m) as bf16 pairs over the S columns in TMEM
         uint32_t pk[32];
         float psum = 0.f;
+        const float neg_m = -m;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float p0 = sv[2 * j] == -CUDART_INF_F ? 0.f : ex2(sv[2 * j] - m);
-          const float p1 = sv[2 * j + 1] == -CUDART_INF_F ? 0.f : ex2(sv[2 * j + 1] - m);
+          float p0 = ex2(fmaf(sv[2 * j], sl2, neg_m));
+          float p1 = ex2(fmaf(sv[2 * j + 1], sl2, neg_m));
+          if (!all_live) {
+            p0 = ((mask >> (2 * j)) & 1ull) ? p0 : 0.f;
+            p1 = ((mask >> (2 * j + 1)) & 1ull) ? p1 : 0.f;
+          }
+          psum += p0 + p1;
           pk[j] = pack_bf16(p0, p1);
-          psum += __bfloat162float(__ushort_as_bfloat16((uint16_t)(pk[j] & 0xffff))) +
-                  __bfloat162float(__ushort_as_bfloat16((uint16_t)(pk[j] >> 16)));
         }
         l += psum;
-        {
-          uint32_t r0[16], r1[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            r0[i] = pk[i];
-            r1[i] = pk[16 + i];
-          }
-          tmem_st16(trow + C::kSCol + 64 * b, r0);
-          tmem_st16(trow + C::kSCol + 64 * b + 16, r1);
-          tmem_st_wait();
-        }
+        tmem_st32(trow + C::kSCol + 64 * b, pk);
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&cs->p_full[b]);
         last_c = c;
@@ -661,23 +664,23 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       const float lse = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
       const bool live = row < H;
 #pragma unroll 1
-      for (int col = 0; col < LC; col += 16) {
-        uint32_t r[16];
-        tmem_ld16(trow + col, r);
+      for (int col = 0; col < LC; col += 32) {
+        uint32_t r[32];
+        tmem_ld32(trow + col, r);
         tmem_ld_wait();
         if (!live) continue;
         if (complete) {
-          uint32_t o[8];
+          uint32_t o[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
+          for (int i = 0; i < 16; ++i)
             o[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + row) * L + lat_x0 + col);
-          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         } else {
           float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)(k * 2 + slot) * H + row) * L + lat_x0 + col);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
                                  __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
         }

@@ -43,12 +43,17 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   int my_tiles = 0;
   bool bad = false;
   for (int t = t0; t < t1; ++t) {
-    int lo_b = 0, hi_b = in.B - 1;   // request of token t: last b with offsets[b] <= t
-    while (lo_b < hi_b) {
-      const int mid = (lo_b + hi_b + 1) >> 1;
-      if ((int)in.offsets[mid] <= t) lo_b = mid; else hi_b = mid - 1;
+    // request of token t: last b with offsets[b] <= t (one query per request is
+    // the common case, so try b = t before searching)
+    int b = min(t, in.B - 1);
+    if (!((int)in.offsets[b] <= t && t < (int)in.offsets[b + 1])) {
+      int lo_b = 0, hi_b = in.B - 1;
+      while (lo_b < hi_b) {
+        const int mid = (lo_b + hi_b + 1) >> 1;
+        if ((int)in.offsets[mid] <= t) lo_b = mid; else hi_b = mid - 1;
+      }
+      b = lo_b;
     }
-    const int b = lo_b;
     const int qb = (int)in.offsets[b], qe = (int)in.offsets[b + 1];
     int lo = 0, hi = 0;
     bool ok = qb <= t && t < qe && (int)in.offsets[in.B] == in.T;
@@ -101,14 +106,15 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   for (int t = t0; t < t1; ++t) in.plan[t].tile_start += base;
   for (int i = tid; i < 2 * in.T; i += nthr) in.counters[i] = 0;
   if (tid == nthr - 1) in.hdr->total_tiles = base + my_tiles;
-  __syncthreads();
-  // tokens with no key: zero latent output and lse = -inf (the decode never visits them)
-  for (int t = 0; t < in.T; ++t) {
+  // tokens with no key: zero latent output and lse = -inf (the decode never visits
+  // them); each thread clears its own tokens
+  for (int t = t0; t < t1; ++t) {
     if (in.plan[t].ntiles != 0) continue;
-    for (int i = tid; i < in.H * in.L; i += nthr)
-      in.o_lat[(size_t)t * in.H * in.L + i] = __float2bfloat16_rn(0.f);
-    for (int i = tid; i < in.H; i += nthr) in.lse_ws[(size_t)t * in.H + i] = -CUDART_INF_F;
+    uint4* o = reinterpret_cast<uint4*>(in.o_lat + (size_t)t * in.H * in.L);
+    for (int i = 0; i < in.H * in.L / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < in.H; ++i) in.lse_ws[(size_t)t * in.H + i] = -CUDART_INF_F;
   }
+  __syncthreads();
   if (tid == 0 && any_bad) atomicOr(&in.hdr->status, kDeviceCheckFailed);
 }
 
