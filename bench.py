@@ -38,7 +38,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 LAUNCHES_PER_CALL = 3       # absorb (+ plan), decode (+ split merge), W_uv
 CPU_SAMPLE_TOKENS = 48      # oracle sample for the CPU baseline (a few seconds of wall time)
 REF_SAMPLE_TOKENS = 2       # oracle sample per step of the reference arm
-KERNEL_SOURCES = {"decode_splitkv": "mla_decode_attention_06_gb300/csrc/mla_decode_simt.cu"}
+KERNEL_SOURCES = {"decode_splitkv": "mla_decode_attention_06_gb300/csrc/mla_decode_tc.cu"}
 
 
 def parse_args():
