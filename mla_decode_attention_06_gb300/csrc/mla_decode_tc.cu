@@ -3,34 +3,42 @@
 // Work split: partition k of K owns the global 64-key tiles [k*Q, (k+1)*Q)
 // (Q = ceil(total/K)); it walks them as segments, one per query token it
 // touches, and writes either the finished latent output (segment = whole
-// token) or a partial (o_p, lse_p) for the combine kernel.  These are the
-// split-KV partitions behind num_partitions_in on the
+// token) or a partial (o_p, lse_p) that the last partition to finish the token
+// merges.  These are the split-KV partitions behind num_partitions_in on the
 // generic_flare_mla_decode_kv_cache_ragged page.
 //
-// One partition runs on a cluster of kCluster CTAs (2 for the 512-wide latent,
-// 1 for narrow latents).  With 128 heads sharing every cached row, scores
-// S = Q . K^T (M = 128 heads, N = 64 keys, K = 576) and the update
-// O += P . C (M = 128, N = 512, K = 64) are dense contractions.  O for 128
-// heads x 512 latent columns in fp32 fills all 512 TMEM columns, so the two
-// CTAs of a cluster split the latent columns: CTA r owns latent columns
-// [256r, 256r + 256) and rope columns [512 + 32r, 512 + 32r + 32).  Each loads
-// only its 288-column slice of every cached row (TMA, 128B / 64B swizzle),
-// computes a partial S over that slice, and the two partial S tiles are
-// exchanged through distributed shared memory; both CTAs then hold the same
-// S = S_0 + S_1 (fp32 addition is commutative, so bit-identical), run the same
-// online softmax, and each applies P to its own 256 latent columns.
+// With 128 heads sharing every cached row, scores S = Q . K^T (M = 128 heads,
+// N = 64 keys, K = 576) and the update O += P . C (M = 128, N = 512, K = 64) are
+// dense contractions.  O for 128 heads x 512 latent columns in fp32 would fill all
+// 512 TMEM columns, so one partition runs on a cluster of two CTAs that split
+// the latent columns of O: CTA r owns columns [256r, 256r + 256).  Scores are
+// not split: every cache tile is multicast by TMA into both CTAs (each CTA
+// issues half of the boxes), and both compute the full S for the tile with the
+// same instructions on the same bits, hence the same S, the same online softmax
+// and the same P; each then applies P to its own half of the latent columns.
+// Nothing is exchanged between the two CTAs but the tiles and the "stage free"
+// signals (tcgen05.commit multicast to both CTAs' empty barriers).
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: query slice once per segment, cache tiles
-//               through the page table into a kStages-deep ring.
-//   warp 1      TMEM owner and MMA issuer (one thread); its other lanes zero
+// The absorbed query (576 columns per head) is split between TMEM and shared
+// memory: latent columns [0, 256) sit in TMEM as the A operand of
+// tcgen05.mma (bf16 pairs), latent [256, 512) and the rope columns in
+// 128B-swizzled shared memory.  TMEM: O (256) | S, two 64-column buffers |
+// Q latent (128).  Narrow latents (64) run the same code on one CTA.
+//
+// Warp roles (224 threads; 288 with the converter warps of an e4m3 cache):
+//   warp 0      TMA producer: the query's shared-memory part once per segment,
+//               cache tiles through the page table into a kStages-deep ring,
+//               and an L2 prefetch of the tile two ahead.
+//   warp 1      TMEM owner and QK issuer (one thread); its other lanes zero
 //               cache rows outside the key range before the MMAs read them
 //               (0 * NaN would poison P . C).
-//   warps 2-5   softmax: thread = head row = TMEM lane.  Reads S, exchanges
-//               partial S, masks, keeps running max / sum in the log2
-//               domain, writes P (bf16 pairs) back into TMEM where the PV MMA
-//               takes it as its A operand, rescales O only when the running
+//   warps 2-5   softmax: thread = head row = TMEM lane.  Writes the query's
+//               TMEM part, reads S, masks, keeps running max / sum in the log2
+//               domain, writes P (bf16 pairs) back into TMEM where the P . C
+//               MMA takes it as its A operand, rescales O only when the running
 //               max grows by more than 2^8, and writes the segment's output.
+//   warps 6-7   (e4m3 cache) widen the tile's codes x row scale into bf16.
+//   last warp   P . C issuer (one thread), so a ready P never waits behind a QK.
 // Every wait is bounded in time; a timeout sets a status bit and the kernel
 // unwinds without hanging.
 #include <math_constants.h>
@@ -43,56 +51,67 @@ namespace tc {
 
 using namespace sm100;
 
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;
 
 // How cache rows reach shared memory.
 enum LoadMode : int {
-  kLoadDense = 0,   // bf16 pool through the page table, TMA tiles
-  kLoadFp8 = 1,     // e4m3 pool through the page table: TMA bytes, widened in place by converter warps
-  kLoadSparse = 2,  // bf16 pool rows named by an index list, TMA gather4
+  kLoadDense = 0,   // bf16 pool through the page table, TMA tiles multicast to the cluster
+  kLoadFp8 = 1,     // e4m3 pool through the page table: TMA bytes (multicast), widened by converter warps
+  kLoadSparse = 2,  // bf16 pool rows named by an index list, TMA gather4 (each CTA its own)
 };
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-template <int kLatentPerCta, int kCluster, int kMode>
-struct Cfg {
-  static constexpr int kThreads = kMode == kLoadFp8 ? 256 : 192;   // + 2 converter warps for e4m3
-  static constexpr int LC = kLatentPerCta;          // latent columns owned by one CTA
-  static constexpr int NLB = LC / 64;               // 64-column (128 B) latent boxes
-  static constexpr int RC = 32;                     // rope box columns (64 B)
-  static constexpr int kLatBoxKv = 64 * 128;        // 64 rows x 128 B
-  static constexpr int kRopeBoxKv = 64 * 64;        // 64 rows x 64 B
-  static constexpr int kStageBytes = NLB * kLatBoxKv + kRopeBoxKv;
-  static constexpr int kLatBoxQ = 128 * 128;
-  static constexpr int kQBytes = NLB * kLatBoxQ + 128 * 64;
-  static constexpr int kXBytes = kCluster == 2 ? 128 * 64 * 4 : 0;
-  static constexpr int kTmemCols = (LC + 128) <= 256 ? 256 : 512;
-  static constexpr int kSCol = LC;                  // S buffers after O
-  static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + kXBytes + 1024;
-  static_assert(LC % 64 == 0 && LC <= 256, "latent slice");
-};
-
-struct Smem {   // control block at the end of dynamic shared memory
-  uint64_t kv_full[kStages], kv_empty[kStages];
+struct Smem {   // control block after the stage ring
+  uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
+  uint64_t kv_conv[kMaxStages];  // e4m3 rows widened (kLoadFp8)
+  uint64_t row_mask[kMaxStages];
   uint64_t q_full, q_empty;
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_free;
-  uint64_t x_full, x_empty;
-  uint64_t kv_conv[kStages];     // e4m3 rows widened (kLoadFp8)
-  uint64_t conv_sync;            // converters: every row read before any is overwritten
+  uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
   uint64_t fix_bar, fix_done;    // softmax: partial written / merge decision published
+  uint64_t mrg_full, mrg_done;   // merge: a partial landed in the idle stage ring / was read
   uint64_t bye;                  // the peer CTA is done touching this CTA's shared memory
-  uint64_t row_mask[kStages];
-  int32_t rowid[kStages][64];    // physical row of each tile row (kLoadFp8, kLoadSparse)
+  int32_t rowid[kMaxStages][64]; // physical row of each tile row (kLoadFp8, kLoadSparse)
   uint32_t tmem_base;
   int abort;
   int fix_last;   // this CTA merges the split token it just finished
 };
 
+template <int kLatentPerCta, int kCluster, int kMode>
+struct Cfg {
+  static constexpr int CL = kCluster;
+  static constexpr int LC = kLatentPerCta;          // latent columns of O owned by one CTA
+  static constexpr int L = LC * CL;                 // latent width
+  static constexpr int NLB = L / 64;                // 64-column latent boxes per cached row
+  static constexpr int kBox = 64 * 128;             // one 128B-swizzled box: 64 rows x 128 B
+  static constexpr int kStageBytes = (NLB + 1) * kBox;   // latent boxes + one rope box
+  static constexpr int kStages = CL == 2 ? 2 : kMaxStages;
+  static constexpr int QT = L < 256 ? L : 256;      // latent columns of the query held in TMEM
+  static constexpr int NQS = (L - QT) / 64;         // latent boxes of the query in shared memory
+  static constexpr int kQBox = 128 * 128;           // 128 rows x 128 B
+  static constexpr int kQBytes = (NQS + 1) * kQBox; // + the rope box
+  static constexpr int kSCol = LC;                  // two 64-column S buffers after O
+  static constexpr int kQCol = LC + 128;            // query latent [0, QT) as bf16 pairs
+  static constexpr int kTmemCols = (kQCol + QT / 2) <= 256 ? 256 : 512;
+  static constexpr int RW = L < 256 ? L : 256;      // e4m3 bytes per raw box row
+  static constexpr int NRH = L / RW;                // raw boxes per cached row
+  static constexpr int kRawOff = NLB >= 8 ? 4 * kBox : 0;   // codes land where the last latent boxes go
+  static constexpr int kConvThreads = 64;                      // warps 6-7 (kLoadFp8)
+  static constexpr int kPvWarp = kMode == kLoadFp8 ? 8 : 6;    // the P . C issuer
+  static constexpr int kThreads = 32 * (kPvWarp + 1);
+  static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + (int)sizeof(Smem);
+  static_assert(LC % 64 == 0 && (CL == 1 || CL == 2), "latent slice");
+  static_assert(kQCol + QT / 2 <= 512, "TMEM columns");
+  static_assert(NRH % CL == 0, "raw boxes split over the cluster");
+  static_assert(kSmem <= 232448, "shared memory");
+};
+
 struct Maps {
-  CUtensorMap kv_lat;    // bf16 latent boxes (kLoadDense: ps rows, kLoadSparse: 1 row) / e4m3 bytes (kLoadFp8)
+  CUtensorMap kv_lat;    // bf16 latent boxes (dense: page rows, sparse: 1 row) / e4m3 bytes (kLoadFp8)
   CUtensorMap kv_rope;   // bf16 rope box
-  CUtensorMap q_lat, q_rope;
+  CUtensorMap q;         // absorbed queries [T * 128, L + R], 64-column boxes
 };
 
 // Walks the segments of partition k: calls f(t, plan, first_tile, end_tile, g_first).
@@ -175,41 +194,59 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Partials of split tokens are stored interleaved, [partition, slot, L / 4, H]
+// float4: a warp's 32 head rows of one 4-column chunk are 512 contiguous bytes,
+// and one CTA's latent half of one partial is a single contiguous block.
+__device__ __forceinline__ size_t part_index(int k, int slot, int c, int row, int L, int H) {
+  return ((size_t)(k * 2 + slot) * (L / 4) + c) * H + row;
+}
+
 // Log-sum-exp merge of one split token's partials for head `row`, latent
 // columns [lat_x0, lat_x0 + LC):  lse = ln sum_p e^{lse_p},
 // o = sum_p e^{lse_p - lse} o_p.  Partitions with an empty key set carry
 // lse_p = -inf and drop out.  Partition k holds the token in slot 0 (its
-// first segment) unless the token began inside partition kf's range.
+// first segment) unless the token began inside partition kf's range.  This is
+// the general form, every partial read from global memory; the common case
+// (the merging CTA's own partial still in TMEM, its stage ring idle) runs in
+// the softmax epilogue instead.
 __device__ __noinline__ void merge_split_token(const DecodeArgs& a, int t, const TokenPlan& tp, int kf, int kl,
                                                int Qt, uint32_t rank, int row, int lat_x0, int LC) {
   const int H = a.d.num_heads, L = a.d.kv_lora_rank;
+  const float4* __restrict__ part_o = reinterpret_cast<const float4*>(a.part_o);
+  const float* __restrict__ part_lse = a.part_lse;
   auto slot_of = [&](int k) { return (k == kf && tp.tile_start != k * Qt) ? 1 : 0; };
+  auto lse_of = [&](int k) { return __ldcg(part_lse + ((size_t)(k * 2 + slot_of(k)) * 2 + rank) * H + row); };
   float mx = -CUDART_INF_F;
-  for (int k = kf; k <= kl; ++k)
-    mx = fmaxf(mx, __ldcg(a.part_lse + ((size_t)(k * 2 + slot_of(k)) * 2 + rank) * H + row));
+  for (int k = kf; k <= kl; ++k) mx = fmaxf(mx, lse_of(k));
   float sum = 0.f;
   if (mx != -CUDART_INF_F)
-    for (int k = kf; k <= kl; ++k)
-      sum += __expf(__ldcg(a.part_lse + ((size_t)(k * 2 + slot_of(k)) * 2 + rank) * H + row) - mx);
+    for (int k = kf; k <= kl; ++k) sum += __expf(lse_of(k) - mx);
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
-  for (int col = 0; col < LC; col += 8) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int col0 = 0; col0 < LC; col0 += 32) {
+    float4 acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (mx != -CUDART_INF_F) {
       for (int k = kf; k <= kl; ++k) {
-        const size_t src = (size_t)(k * 2 + slot_of(k)) * H + row;
-        const float w = __expf(__ldcg(a.part_lse + ((size_t)(k * 2 + slot_of(k)) * 2 + rank) * H + row) - mx) * inv;
-        const float4* p = reinterpret_cast<const float4*>(a.part_o + src * L + lat_x0 + col);
-        const float4 u = __ldcg(p), v = __ldcg(p + 1);
-        acc[0] += w * u.x; acc[1] += w * u.y; acc[2] += w * u.z; acc[3] += w * u.w;
-        acc[4] += w * v.x; acc[5] += w * v.y; acc[6] += w * v.z; acc[7] += w * v.w;
+        const float w = __expf(lse_of(k) - mx) * inv;
+        const int c0 = (lat_x0 + col0) / 4;
+        float4 u[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) u[i] = __ldcg(part_o + part_index(k, slot_of(k), c0 + i, row, L, H));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[i].x = fmaf(w, u[i].x, acc[i].x);
+          acc[i].y = fmaf(w, u[i].y, acc[i].y);
+          acc[i].z = fmaf(w, u[i].z, acc[i].z);
+          acc[i].w = fmaf(w, u[i].w, acc[i].w);
+        }
       }
     }
-    uint4 o;
-    o.x = pack_bf16(acc[0], acc[1]);
-    o.y = pack_bf16(acc[2], acc[3]);
-    o.z = pack_bf16(acc[4], acc[5]);
-    o.w = pack_bf16(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + row) * L + lat_x0 + col) = o;
+    uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + row) * L + lat_x0 + col0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      dst[i] = make_uint4(pack_bf16(acc[2 * i].x, acc[2 * i].y), pack_bf16(acc[2 * i].z, acc[2 * i].w),
+                          pack_bf16(acc[2 * i + 1].x, acc[2 * i + 1].y), pack_bf16(acc[2 * i + 1].z, acc[2 * i + 1].w));
   }
   if (rank == 0) a.lse_ws[(size_t)t * H + row] = mx != -CUDART_INF_F ? mx + __logf(sum) : -CUDART_INF_F;
 }
@@ -226,6 +263,95 @@ __device__ __forceinline__ bool wwait_cluster(uint64_t* bar, uint32_t parity, Sm
 }
 __device__ __forceinline__ bool waborted(const Smem* cs) { return __any_sync(0xffffffffu, aborted(cs)); }
 
+// The merge of a split token by a CTA whose last segment it was: O in TMEM
+// still holds this CTA's own partial (unnormalised; 1 / row sum = inv) and the
+// stage ring is idle.  Each other partition's slice of its partial (one
+// contiguous block of the interleaved layout) comes in with one bulk copy into
+// the ring.  acc = sum over partitions, in order, of fmaf(w_p, o_p, acc) from
+// zero: the operations and order of merge_split_token, so the bits do not
+// depend on which partition merges.  acc lives in TMEM at `tacc` (the S and
+// query columns, idle after the last QK).  Warp-uniform; false on a time-out.
+__device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t, const TokenPlan& tp, int k, int kf,
+                                           int kl, int Qt, uint32_t rank, int row, int lat_x0, int LC, uint32_t trow,
+                                           uint32_t tacc, float lse_own, float inv, uint8_t* ring, int& nmrg) {
+  const int H = a.d.num_heads, L = a.d.kv_lora_rank;
+  PlanHeader* hdr = a.hdr_mut;
+  const bool live = row < H;
+  auto slot_of = [&](int kk) { return (kk == kf && tp.tile_start != kk * Qt) ? 1 : 0; };
+  auto lse_of = [&](int kk) {
+    return kk == k ? lse_own : __ldcg(a.part_lse + ((size_t)(kk * 2 + slot_of(kk)) * 2 + rank) * H + row);
+  };
+  float mx = -CUDART_INF_F;
+  for (int kk = kf; kk <= kl; ++kk) mx = fmaxf(mx, lse_of(kk));
+  float sum = 0.f;
+  if (mx != -CUDART_INF_F)
+    for (int kk = kf; kk <= kl; ++kk) sum += __expf(lse_of(kk) - mx);
+  const float inv_sum = sum > 0.f ? 1.f / sum : 0.f;
+  const float4* sp = reinterpret_cast<const float4*>(ring);
+  for (int kk = kf; kk <= kl; ++kk) {
+    const float w = mx != -CUDART_INF_F ? __expf(lse_of(kk) - mx) * inv_sum : 0.f;
+    const bool own = kk == k, first = kk == kf;
+    if (!own) {
+      bool ok = true;
+      if (row == 0) {
+        if (nmrg > 0) ok = wait_or_abort(&cs->mrg_done, (nmrg - 1) & 1, cs, hdr);
+        if (ok) {
+          const uint32_t bytes = (uint32_t)(LC * H * 4);
+          fence_proxy_async_global();
+          mbar_arrive_expect_tx(&cs->mrg_full, bytes);
+          bulk_copy_g2s(ring, reinterpret_cast<const float4*>(a.part_o) + part_index(kk, slot_of(kk), lat_x0 / 4, 0, L, H),
+                        bytes, &cs->mrg_full);
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      if (!wwait(&cs->mrg_full, nmrg & 1, cs, hdr)) return false;
+    }
+#pragma unroll 1
+    for (int col = 0; col < LC; col += 16) {
+      uint32_t u[16], acc[16];
+      if (own) tmem_ld16(trow + col, u);
+      if (!first) tmem_ld16(tacc + col, acc);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float v[4];
+        if (own) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(u[4 * i + j]) * inv;
+        } else {
+          const float4 x = live ? sp[(col / 4 + i) * H + row] : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          acc[4 * i + j] = __float_as_uint(fmaf(w, v[j], first ? 0.f : __uint_as_float(acc[4 * i + j])));
+      }
+      tmem_st16(tacc + col, acc);
+    }
+    tmem_st_wait();
+    if (!own) {
+      mbar_arrive(&cs->mrg_done);
+      ++nmrg;
+    }
+  }
+  // the merged row: bf16 latent output and its log-sum-exp
+#pragma unroll 1
+  for (int col = 0; col < LC; col += 16) {
+    uint32_t r[16];
+    tmem_ld16(tacc + col, r);
+    tmem_ld_wait();
+    if (!live) continue;
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+    uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + row) * L + lat_x0 + col);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  if (live && rank == 0) a.lse_ws[(size_t)t * H + row] = mx != -CUDART_INF_F ? mx + __logf(sum) : -CUDART_INF_F;
+  return true;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -237,32 +363,32 @@ template <int LC, int CL, int MODE>
 __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ Maps maps, const DecodeArgs a) {
   using C = Cfg<LC, CL, MODE>;
+  constexpr int S = C::kStages;
+  constexpr int L = C::L;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* sQ = sm;
-  uint8_t* sStage = sQ + C::kQBytes;
-  float* sX = reinterpret_cast<float*>(sStage + kStages * C::kStageBytes);
-  Smem* cs = reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sX) + C::kXBytes);
+  uint8_t* sQ = sm;                                  // query latent [QT, L) boxes, then the rope box
+  uint8_t* sStage = sQ + C::kQBytes;                 // S stages of NLB latent boxes + 1 rope box
+  Smem* cs = reinterpret_cast<Smem*>(sStage + S * C::kStageBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = CL == 2 ? cluster_ctarank() : 0u;
   const uint32_t peer = rank ^ 1u;
   const int k = blockIdx.x / CL;
   PlanHeader* hdr = a.hdr_mut;
-  const int L = a.d.kv_lora_rank, H = a.d.num_heads;
+  const int H = a.d.num_heads;
+  const int KQ = L + a.d.qk_rope;
   const int lat_x0 = (int)rank * LC;
-  // this CTA's rope columns: in the absorbed query row they start at L; in the
-  // cache they start at L too, except in the e4m3 pool's bf16 view (L / 2)
-  const int q_rope_x0 = L + (int)rank * (a.d.qk_rope / CL);
-  const int rope_x0 = (MODE == kLoadFp8 ? L / 2 : L) + (int)rank * (a.d.qk_rope / CL);
+  // cache rope columns: they start at L in a bf16 row, at byte L (bf16 column L / 2) in an e4m3 row
+  const int rope_x0 = MODE == kLoadFp8 ? L / 2 : L;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&cs->kv_full[s], 1);
-      mbar_init(&cs->kv_empty[s], 1);
-      mbar_init(&cs->kv_conv[s], 64);
+      mbar_init(&cs->kv_empty[s], CL);   // one tcgen05.commit from each CTA of the cluster
+      mbar_init(&cs->kv_conv[s], C::kConvThreads);
     }
-    mbar_init(&cs->q_full, 1);
+    mbar_init(&cs->q_full, 1 + 128);     // producer (TMA bytes) + every softmax thread (TMEM part)
     mbar_init(&cs->q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&cs->s_full[b], 1);
@@ -270,11 +396,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       mbar_init(&cs->pv_done[b], 1);
     }
     mbar_init(&cs->o_free, 128);
-    mbar_init(&cs->x_full, 1);   // expect_tx by row 0 + 32 KB of st.async from the peer
-    mbar_init(&cs->x_empty, 128);
-    mbar_init(&cs->conv_sync, 64);
+    mbar_init(&cs->conv_sync, C::kConvThreads);
     mbar_init(&cs->fix_bar, 128);
     mbar_init(&cs->fix_done, 1);
+    mbar_init(&cs->mrg_full, 1);
+    mbar_init(&cs->mrg_done, 128);
     mbar_init(&cs->bye, 1);
     cs->abort = 0;
     fence_mbar_init();
@@ -286,10 +412,10 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&maps.kv_lat);
     prefetch_tensormap(&maps.kv_rope);
-    prefetch_tensormap(&maps.q_lat);
-    prefetch_tensormap(&maps.q_rope);
+    prefetch_tensormap(&maps.q);
   }
   tc_fence_before();
+  // both CTAs' barriers are initialised before either multicasts into the other
   if (CL == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = cs->tmem_base;
@@ -305,34 +431,31 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
+    auto load_box = [&](void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+      if (CL == 2) tma_load_2d_mc(dst, map, bar, x, y, (uint16_t)0x3);
+      else tma_load_2d(dst, map, bar, x, y);
+    };
     int c = 0;
     bool bad = false;
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
-      if (waborted(cs)) return;
-      if (si > 0 && !wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&cs->q_full, C::kQBytes);
-        for (int i = 0; i < C::NLB; ++i)
-          tma_load_2d(sQ + i * C::kLatBoxQ, &maps.q_lat, &cs->q_full, lat_x0 + 64 * i, t * kMaxHeads);
-        tma_load_2d(sQ + C::NLB * C::kLatBoxQ, &maps.q_rope, &cs->q_full, q_rope_x0, t * kMaxHeads);
-      }
-      for (int it = ia; it < ie; ++it, ++c) {
-        if (waborted(cs)) return;
-        const int s = c % kStages;
-        if (c >= kStages && !wwait(&cs->kv_empty[s], ((c / kStages) & 1) ^ 1, cs, hdr)) return;
+      bool q_pending = true;   // the query's shared-memory part goes right after the first tile
+      constexpr int kOwn = MODE == kLoadFp8 ? C::NRH / CL : C::NLB / CL;   // this CTA's boxes per load
+      const int nloads = kTileKeys / rows_per_load;
+      const uint64_t lmask = rows_per_load == 64 ? ~0ull : ((1ull << rows_per_load) - 1);
+      // rows j and j + 32 of tile `it`: which key / slot, and is it live?
+      auto lookup = [&](int it, bool (&v)[2], int (&rid)[2], int (&pg)[2]) {
         const int key0 = (tp.tile_first + it) * kTileKeys;
-        // rows j and j + 32 of this tile: which key / slot, and is it live?
-        bool v[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int key = key0 + lane + 32 * h;
           bool ok = key >= tp.lo && key < tp.hi;
-          int rid = 0;
+          rid[h] = 0;
+          pg[h] = 0;
           if (ok) {
             if (MODE == kLoadSparse) {
               const int idx = a.ks.indices[(size_t)tp.b * a.ks.idx_stride + key];
               if (idx >= 0 && idx < a.ks.num_pages * ps) {
-                rid = idx;
+                rid[h] = idx;
               } else {
                 ok = false;
                 if (idx != -1) bad = true;
@@ -340,21 +463,65 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             } else {
               const int page = a.ks.block_table[(size_t)tp.b * a.ks.bt_stride + key / ps];
               if (page < 0 || page >= a.ks.num_pages) { ok = false; bad = true; }
-              else rid = page * ps + key % ps;
+              else { pg[h] = page; rid[h] = page * ps + key % ps; }
             }
           }
           v[h] = ok;
-          if (MODE != kLoadDense) cs->rowid[s][lane + 32 * h] = rid;
+        }
+      };
+      // the pool row of load p of a tile, from the lane that looked up its first live row
+      auto load_row = [&](int it, int p, uint64_t pm, const int (&pg)[2]) {
+        const int r0 = p * rows_per_load;
+        const int fr = r0 + __ffsll((long long)pm) - 1;
+        const int pa = __shfl_sync(0xffffffffu, pg[0], fr & 31);
+        const int pb = __shfl_sync(0xffffffffu, pg[1], fr & 31);
+        const int page = fr < 32 ? pa : pb;
+        return page * ps + ((tp.tile_first + it) * kTileKeys + r0) % ps;
+      };
+      // L2 prefetch of this CTA's boxes of tile `it` (paged modes): its load, issued
+      // when a stage frees up, then reads L2 instead of waiting on HBM
+      auto prefetch = [&](int it) {
+        if (MODE == kLoadSparse || it >= ie) return;
+        bool v[2];
+        int rid[2], pg[2];
+        lookup(it, v, rid, pg);
+        const uint64_t mask = (uint64_t)__ballot_sync(0xffffffffu, v[0]) |
+                              ((uint64_t)__ballot_sync(0xffffffffu, v[1]) << 32);
+        for (int p = 0; p < nloads; ++p) {
+          const uint64_t pm = (mask >> (p * rows_per_load)) & lmask;
+          if (!pm) continue;
+          const int y = load_row(it, p, pm, pg);
+          if (lane < kOwn) {
+            if (MODE == kLoadFp8) tma_prefetch_2d(&maps.kv_lat, ((int)rank * kOwn + lane) * C::RW, y);
+            else tma_prefetch_2d(&maps.kv_lat, 64 * ((int)rank * kOwn + lane), y);
+          } else if (lane == kOwn && rank == 0) {
+            tma_prefetch_2d(&maps.kv_rope, rope_x0, y);
+          }
+        }
+      };
+      if (ia + 1 < ie) prefetch(ia + 1);
+      for (int it = ia; it < ie; ++it, ++c) {
+        if (waborted(cs)) return;
+        const int s = c % S;
+        // global reads, issued before the wait for the stage so their latency overlaps it
+        bool v[2];
+        int rid[2], pg[2];
+        lookup(it, v, rid, pg);
+        // stage s is free in both CTAs once both have committed their P . C of its last tile
+        if (c >= S && !wwait(&cs->kv_empty[s], ((c / S) & 1) ^ 1, cs, hdr)) return;
+        if (MODE != kLoadDense) {
+          cs->rowid[s][lane] = rid[0];
+          cs->rowid[s][lane + 32] = rid[1];
         }
         const uint64_t mask = (uint64_t)__ballot_sync(0xffffffffu, v[0]) |
                               ((uint64_t)__ballot_sync(0xffffffffu, v[1]) << 32);
         uint8_t* st = sStage + s * C::kStageBytes;
-        uint8_t* st_rope = st + C::NLB * C::kLatBoxKv;
+        uint8_t* st_rope = st + C::NLB * C::kBox;
         if (MODE == kLoadSparse) {
-          // every row is fetched (row 0 stands in for a dead slot and is zeroed before use)
+          // every row is fetched by each CTA (row 0 stands in for a dead slot; its P . C part is zeroed)
           if (lane == 0) {
             cs->row_mask[s] = mask;
-            mbar_arrive_expect_tx(&cs->kv_full[s], 64 * (C::NLB * 128 + 64));
+            mbar_arrive_expect_tx(&cs->kv_full[s], 64 * (C::NLB + 1) * 128);
           }
           __syncwarp();
           if (lane < 16) {
@@ -363,177 +530,212 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             const int y2 = cs->rowid[s][r0 + 2], y3 = cs->rowid[s][r0 + 3];
 #pragma unroll
             for (int i = 0; i < C::NLB; ++i)
-              tma_gather4(st + i * C::kLatBoxKv + r0 * 128, &maps.kv_lat, &cs->kv_full[s], lat_x0 + 64 * i, y0, y1, y2, y3);
-            tma_gather4(st_rope + r0 * 64, &maps.kv_rope, &cs->kv_full[s], rope_x0, y0, y1, y2, y3);
+              tma_gather4(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y0, y1, y2, y3);
+            tma_gather4(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y0, y1, y2, y3);
           }
-        } else if (lane == 0) {
-          cs->row_mask[s] = mask;
-          // pages of this tile that hold at least one live row
-          const int nloads = kTileKeys / rows_per_load;
-          const uint32_t row_bytes = MODE == kLoadFp8 ? (LC + 64) : (C::NLB * 128 + 64);
-          uint32_t bytes = 0;
-          for (int p = 0; p < nloads; ++p) {
-            const uint64_t pm = (rows_per_load == 64) ? mask : ((mask >> (p * rows_per_load)) & ((1ull << rows_per_load) - 1));
-            if (pm) bytes += rows_per_load * row_bytes;
+        } else {
+          // pages of this tile that hold at least one live row; both CTAs count the
+          // same bytes, half of which the peer's multicast delivers
+          const uint32_t row_bytes = (MODE == kLoadFp8 ? L : C::NLB * 128) + 128;
+          if (lane == 0) {
+            cs->row_mask[s] = mask;
+            uint32_t bytes = 0;
+            for (int p = 0; p < nloads; ++p)
+              if ((mask >> (p * rows_per_load)) & lmask) bytes += rows_per_load * row_bytes;
+            mbar_arrive_expect_tx(&cs->kv_full[s], bytes);
           }
-          mbar_arrive_expect_tx(&cs->kv_full[s], bytes);
+          __syncwarp();
           for (int p = 0; p < nloads; ++p) {
-            const uint64_t pm = (rows_per_load == 64) ? mask : ((mask >> (p * rows_per_load)) & ((1ull << rows_per_load) - 1));
+            const uint64_t pm = (mask >> (p * rows_per_load)) & lmask;
             if (!pm) continue;
-            const int kp = key0 + p * rows_per_load;
-            const int page = a.ks.block_table[(size_t)tp.b * a.ks.bt_stride + kp / ps];
-            const int y = page * ps + kp % ps;
             const int r0 = p * rows_per_load;
-            if (MODE == kLoadFp8) {
-              // raw e4m3 rows (LC bytes each) at the start of the stage, widened later
-              tma_load_2d(st + r0 * LC, &maps.kv_lat, &cs->kv_full[s], lat_x0, y);
-            } else {
-              for (int i = 0; i < C::NLB; ++i)
-                tma_load_2d(st + i * C::kLatBoxKv + r0 * 128, &maps.kv_lat, &cs->kv_full[s], lat_x0 + 64 * i, y);
+            const int y = load_row(it, p, pm, pg);
+            // one box per lane: this CTA's share of the latent (or raw e4m3) boxes, then the rope box (rank 0)
+            if (lane < kOwn) {
+              if (MODE == kLoadFp8) {
+                const int h = (int)rank * kOwn + lane;
+                load_box(st + C::kRawOff + h * 64 * C::RW + r0 * C::RW, &maps.kv_lat, &cs->kv_full[s], h * C::RW, y);
+              } else {
+                const int i = (int)rank * kOwn + lane;
+                load_box(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y);
+              }
+            } else if (lane == kOwn && rank == 0) {
+              load_box(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y);
             }
-            tma_load_2d(st_rope + r0 * 64, &maps.kv_rope, &cs->kv_full[s], rope_x0, y);
           }
+          prefetch(it + 2);
         }
         __syncwarp();
+        if (q_pending) {
+          // the previous segment's last QK has read the query buffers
+          if (si > 0 && !wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&cs->q_full, C::kQBytes);
+            for (int i = 0; i < C::NQS; ++i)
+              tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->q_full, C::QT + 64 * i, t * kMaxHeads);
+            tma_load_2d(sQ + C::NQS * C::kQBox, &maps.q, &cs->q_full, L, t * kMaxHeads);
+          }
+          __syncwarp();
+          q_pending = false;
+        }
       }
     });
     if (bad) atomicOr(&hdr->status, kDeviceCheckFailed);
-    // make sure no TMA write is still in flight when the CTA leaves
+    // no TMA write of ours still in flight, and (cluster) no commit of the peer
+    // still to arrive on our barriers, when the CTA leaves
     if (lane == 0) {
-      for (int j = c - kStages; j < c; ++j) {
+      for (int j = c - S; j < c; ++j) {
         if (j < 0) continue;
-        mbar_wait(&cs->kv_full[j % kStages], (j / kStages) & 1, kWaitLimitNs);
+        mbar_wait(&cs->kv_full[j % S], (j / S) & 1, kWaitLimitNs);
+        if (CL == 2) mbar_wait(&cs->kv_empty[j % S], (j / S) & 1, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------------- QK issuer
+    // QK of tile c as soon as its rows have landed.  The S buffer of tile c held
+    // P of tile c - 2, which the P . C warp reads: wait for that MMA to complete.
+    // The MMA queue is shallow, so the 36 MMAs are issued back to back.
     const uint32_t idesc_qk = idesc_bf16_f32(128, 64, false, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(128, LC, false, true);
-    const uint32_t sQa = smem_u32(sQ);
-    const uint32_t sSa = smem_u32(sStage);
-    int c = 0;
-    int prev_s = -1, prev_b = -1, prev_c = -1;
-    bool first_pv_of_seg = true;
-    int seg_of_prev = -1;
-    auto issue_pv = [&](int si) {
-      // P(prev) is in TMEM, O is free for the segment's first PV
-      if (!wwait(&cs->p_full[prev_b], (prev_c / 2) & 1, cs, hdr)) return false;
-      if (first_pv_of_seg && si > 0 && !wwait(&cs->o_free, (si - 1) & 1, cs, hdr)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t st = sSa + prev_s * C::kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bd = smem_desc(st + kk * 2048, C::kLatBoxKv, 1024, kLayoutSw128);
-          mma_ts(tmem, tmem + C::kSCol + 64 * prev_b + 8 * kk, bd, idesc_pv,
-                 (first_pv_of_seg && kk == 0) ? 0u : 1u);
-        }
-        mma_commit(&cs->kv_empty[prev_s]);
-        mma_commit(&cs->pv_done[prev_b]);
-      }
-      __syncwarp();
-      first_pv_of_seg = false;
-      return true;
-    };
+    // K-major operand descriptors of the query boxes and of stage 0; the start
+    // address field is advanced by (byte offset >> 4) for every other operand
+    const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSw128);
+    const uint64_t dk0 = smem_desc(smem_u32(sStage), 16, 1024, kLayoutSw128);
+    int cq = 0, nseg = 0;
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
+      nseg = si + 1;
       if (waborted(cs)) return;
       if (!wwait(&cs->q_full, si & 1, cs, hdr)) return;
-      first_pv_of_seg = true;
-      for (int it = ia; it < ie; ++it, ++c) {
+      for (int it = ia; it < ie; ++it, ++cq) {
         if (waborted(cs)) return;
-        const int s = c % kStages, b = c & 1;
-        if (MODE == kLoadFp8) {
-          if (!wwait(&cs->kv_conv[s], (c / kStages) & 1, cs, hdr)) return;
-        } else if (!wwait(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) {
-          return;
-        }
+        const int s = cq % S, b = cq & 1;
+        if (!wwait(MODE == kLoadFp8 ? &cs->kv_conv[s] : &cs->kv_full[s], (cq / S) & 1, cs, hdr)) return;
+        if (cq >= 2 && !wwait(&cs->pv_done[b], ((cq - 2) >> 1) & 1, cs, hdr)) return;
         const uint64_t mask = cs->row_mask[s];
         if (MODE != kLoadFp8 && mask != ~0ull) {
-          // zero rows outside the key range in every box of the stage
-          uint8_t* st = sStage + s * C::kStageBytes;
-          const int chunks_per_row = C::NLB * 8 + 4;   // 16-byte chunks
-          for (int i = lane; i < 64 * chunks_per_row; i += 32) {
-            const int row = i / chunks_per_row, ch = i % chunks_per_row;
-            if ((mask >> row) & 1ull) continue;
-            uint8_t* dst = ch < C::NLB * 8 ? st + (ch >> 3) * C::kLatBoxKv + row * 128 + (ch & 7) * 16
-                                           : st + C::NLB * C::kLatBoxKv + row * 64 + (ch - C::NLB * 8) * 16;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+          // Rows outside the key range may hold anything (NaN included).  Their
+          // scores are dropped by the row mask, not by value, so only this CTA's
+          // P . C boxes need them zeroed (P = 0 times NaN would poison O): one
+          // row per step, one 16-byte chunk of its 4 x 128 bytes per lane.
+          uint8_t* vb = sStage + s * C::kStageBytes + (lat_x0 / 64) * C::kBox;
+          constexpr int kVChunks = (LC / 64) * 8;
+          uint64_t dead = ~mask;
+          while (dead) {
+            const int row = __ffsll((long long)dead) - 1;
+            dead &= dead - 1;
+            for (int ch = lane; ch < kVChunks; ch += 32)
+              *reinterpret_cast<uint4*>(vb + (ch >> 3) * C::kBox + row * 128 + (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t st = sSa + s * C::kStageBytes;
-          int j = 0;
+          const uint64_t dk = dk0 + (uint64_t)((s * C::kStageBytes) >> 4);
+          const uint32_t sd = tmem + C::kSCol + 64 * b;
+          // latent [0, QT): A = query in TMEM
 #pragma unroll
-          for (int i = 0; i < C::NLB; ++i) {
+          for (int kk = 0; kk < C::QT / 16; ++kk)
+            mma_ts(sd, tmem + C::kQCol + 8 * kk, dk + (uint64_t)(((kk >> 2) * C::kBox + (kk & 3) * 32) >> 4),
+                   idesc_qk, kk > 0 ? 1u : 0u);
+          // latent [QT, L): A = query boxes in shared memory
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk, ++j) {
-              const uint64_t ad = smem_desc(sQa + i * C::kLatBoxQ + kk * 32, 16, 1024, kLayoutSw128);
-              const uint64_t bd = smem_desc(st + i * C::kLatBoxKv + kk * 32, 16, 1024, kLayoutSw128);
-              mma_ss(tmem + C::kSCol + 64 * b, ad, bd, idesc_qk, j > 0 ? 1u : 0u);
-            }
+          for (int i = 0; i < C::NQS; ++i) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(sd, dq0 + (uint64_t)((i * C::kQBox + kk * 32) >> 4),
+                     dk + (uint64_t)(((C::QT / 64 + i) * C::kBox + kk * 32) >> 4), idesc_qk, 1u);
           }
+          // rope (64 columns; past qk_rope both sides read the TMA zero fill)
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t ad = smem_desc(sQa + C::NLB * C::kLatBoxQ + kk * 32, 16, 512, kLayoutSw64);
-            const uint64_t bd = smem_desc(st + C::NLB * C::kLatBoxKv + kk * 32, 16, 512, kLayoutSw64);
-            mma_ss(tmem + C::kSCol + 64 * b, ad, bd, idesc_qk, 1u);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(sd, dq0 + (uint64_t)((C::NQS * C::kQBox + kk * 32) >> 4),
+                   dk + (uint64_t)((C::NLB * C::kBox + kk * 32) >> 4), idesc_qk, 1u);
           mma_commit(&cs->s_full[b]);
+          // the segment's last QK: its query buffers may be refilled once it completes
+          if (it + 1 == ie) mma_commit(&cs->q_empty);
         }
         __syncwarp();
-        if (prev_c >= 0 && seg_of_prev == si && !issue_pv(si)) return;
-        prev_s = s;
-        prev_b = b;
-        prev_c = c;
-        seg_of_prev = si;
       }
-      if (prev_c >= 0 && !issue_pv(si)) return;
-      prev_c = -1;
-      if (lane == 0) mma_commit(&cs->q_empty);
-      __syncwarp();
+    });
+    // the last commit lands on this CTA's barrier before the CTA leaves
+    if (lane == 0 && nseg > 0) mbar_wait(&cs->q_empty, (nseg - 1) & 1, kWaitLimitNs);
+    __syncwarp();
+  } else if (warp == C::kPvWarp) {
+    // ------------------------------------------------------------- P . C issuer
+    // O += P . C for tile c as soon as its P is in TMEM (and, for a segment's
+    // first tile, the previous segment's O has been read); the commit frees the
+    // stage in both CTAs of the cluster.
+    const uint32_t idesc_pv = idesc_bf16_f32(128, LC, false, true);
+    const uint64_t dv0 = smem_desc(smem_u32(sStage) + (lat_x0 / 64) * C::kBox, C::kBox, 1024, kLayoutSw128);
+    int cp = 0;
+    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
+      for (int it = ia; it < ie; ++it, ++cp) {
+        if (waborted(cs)) return;
+        const int b = cp & 1;
+        if (!wwait(&cs->p_full[b], (cp >> 1) & 1, cs, hdr)) return;
+        if (it == ia && si > 0 && !wwait(&cs->o_free, (si - 1) & 1, cs, hdr)) return;
+        tc_fence_after();
+        if (lane == 0) {
+          // B = this CTA's latent boxes of the stage, keys along K (MN-major)
+          const uint64_t dv = dv0 + (uint64_t)(((cp % S) * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem, tmem + C::kSCol + 64 * b + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                   (it == ia && kk == 0) ? 0u : 1u);
+          if (CL == 2) mma_commit_mc(&cs->kv_empty[cp % S], (uint16_t)0x3);
+          else mma_commit(&cs->kv_empty[cp % S]);
+          mma_commit(&cs->pv_done[b]);
+        }
+        __syncwarp();
+      }
     });
   } else if (MODE == kLoadFp8 && warp >= 6) {
     // ------------------------------------------------------------- e4m3 converters
-    // thread ci widens tile row ci: LC e4m3 codes x row scale -> bf16 in the
+    // thread ci widens tile row ci: L e4m3 codes x row scale -> bf16 in the
     // 128B-swizzled latent boxes; dead rows become zeros (latent and rope).
+    // The codes sit where the last latent boxes go (L = 512: boxes 4-7; L = 64:
+    // box 0), so every thread reads the codes of the last raw box before anyone
+    // writes those boxes.
     const int ci = tid - 192;
     int c = 0;
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
-        const int s = c % kStages;
-        if (!wwait(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) return;
+        const int s = c % S;
+        if (!wwait(&cs->kv_full[s], (c / S) & 1, cs, hdr)) return;
         uint8_t* st = sStage + s * C::kStageBytes;
         const bool live = (cs->row_mask[s] >> ci) & 1ull;
         const float sc = live ? a.kv_scales[cs->rowid[s][ci]] : 0.f;
-        uint4 raw[LC / 16];
+#pragma unroll 1
+        for (int h = 0; h < C::NRH; ++h) {
+          uint4 raw[C::RW / 16];
+          const uint8_t* src = st + C::kRawOff + h * 64 * C::RW + ci * C::RW;
 #pragma unroll
-        for (int q = 0; q < LC / 16; ++q) raw[q] = *reinterpret_cast<const uint4*>(st + ci * LC + q * 16);
-        // all rows are read before any is overwritten (the codes live where the bf16 rows go)
-        mbar_arrive(&cs->conv_sync);
-        if (!wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
-#pragma unroll
-        for (int q = 0; q < LC / 16; ++q) {
-          const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
-          uint32_t o[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
-            o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
+          for (int q = 0; q < C::RW / 16; ++q) raw[q] = *reinterpret_cast<const uint4*>(src + q * 16);
+          if (h == C::NRH - 1) {
+            mbar_arrive(&cs->conv_sync);
+            if (!wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
           }
-          const int col = 16 * q;                  // first latent column of this chunk pair
-          uint8_t* box = st + (col >> 6) * C::kLatBoxKv + ci * 128;
-          const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
-          *reinterpret_cast<uint4*>(box + (((ch) ^ (ci & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (ci & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+          for (int q = 0; q < C::RW / 16; ++q) {
+            const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
+              o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
+            }
+            const int col = h * C::RW + 16 * q;      // first latent column of this chunk pair
+            uint8_t* box = st + (col >> 6) * C::kBox + ci * 128;
+            const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
+            *reinterpret_cast<uint4*>(box + (((ch) ^ (ci & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (ci & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
         }
         if (!live) {
-          uint4* rr = reinterpret_cast<uint4*>(st + C::NLB * C::kLatBoxKv + ci * 64);
+          uint4* rr = reinterpret_cast<uint4*>(st + C::NLB * C::kBox + ci * 128);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) rr[i] = make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < 8; ++i) rr[i] = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
         mbar_arrive(&cs->kv_conv[s]);
@@ -545,22 +747,44 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const int row = 32 * q + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
     const float sl2 = a.scale * 1.4426950408889634f;
-    uint32_t peer_x = 0, peer_xfull = 0, peer_xempty = 0;
-    if (CL == 2) {
-      peer_x = mapa_shared(smem_u32(sX), peer);
-      peer_xfull = mapa_shared(smem_u32(&cs->x_full), peer);
-      peer_xempty = mapa_shared(smem_u32(&cs->x_empty), peer);
-    }
+    // this head's absorbed query, latent [0, QT), into TMEM as bf16 pairs (low half = even column)
+    auto load_q = [&](int t) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.q_full + ((size_t)t * kMaxHeads + row) * KQ);
+      const bool has = row < H;
+#pragma unroll 1
+      for (int w0 = 0; w0 < C::QT / 2; w0 += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = has ? __ldcg(src + w0 / 4 + i) : make_uint4(0, 0, 0, 0);
+          w[4 * i] = v.x;
+          w[4 * i + 1] = v.y;
+          w[4 * i + 2] = v.z;
+          w[4 * i + 3] = v.w;
+        }
+        tmem_st32(trow + C::kQCol + w0, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&cs->q_full);
+    };
     int c = 0;
     int nfix = 0;   // split-token merges attempted (phase of fix_bar / fix_done)
+    int nmrg = 0;   // partials brought in by bulk copy (phase of mrg_full / mrg_done)
+    bool q_ready = false;   // the coming segment's query is already in TMEM
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg) {
       if (waborted(cs)) return;
+      if (!q_ready) {
+        if (si > 0 && !wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
+        load_q(t);
+      }
+      q_ready = false;
       float m = -CUDART_INF_F, l = 0.f;
       int last_c = -1;
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
-        const int s = c % kStages, b = c & 1;
-        if (!wwait(&cs->kv_full[s], (c / kStages) & 1, cs, hdr)) return;   // row mask visibility
+        const int s = c % S, b = c & 1;
+        if (!wwait(&cs->kv_full[s], (c / S) & 1, cs, hdr)) return;   // row mask visibility
         const uint64_t mask = cs->row_mask[s];
         if (!wwait(&cs->s_full[b], (c >> 1) & 1, cs, hdr)) return;
         tc_fence_after();
@@ -572,27 +796,6 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         float sv[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(sr[j]);
-        if (CL == 2) {
-          // my partial S goes to the peer with asynchronous stores that count bytes on
-          // the peer's x_full; the peer's partial arrives in mine the same way
-          if (c > 0 && !wwait_cluster(&cs->x_empty, (c - 1) & 1, cs, hdr)) return;
-          if (row == 0) mbar_arrive_expect_tx(&cs->x_full, 128 * 64 * 4);
-          const uint32_t dst = peer_x + (uint32_t)(row * 256);
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch)
-            st_async_v4(dst + (uint32_t)((ch ^ (row & 15)) * 16), sr[4 * ch], sr[4 * ch + 1], sr[4 * ch + 2],
-                        sr[4 * ch + 3], peer_xfull);
-          if (!wwait_cluster(&cs->x_full, c & 1, cs, hdr)) return;
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            const float4 pv = *reinterpret_cast<const float4*>(sX + row * 64 + (ch ^ (row & 15)) * 4);
-            sv[4 * ch] += pv.x;
-            sv[4 * ch + 1] += pv.y;
-            sv[4 * ch + 2] += pv.z;
-            sv[4 * ch + 3] += pv.w;
-          }
-          mbar_arrive_cluster(peer_xempty);
-        }
         // row max of the scaled scores (log2 domain); dead keys do not count
         const bool all_live = mask == ~0ull;
         float mx;
@@ -656,6 +859,17 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       }
       if (last_c < 0) return;
       // ------------------------------------------------------------- epilogue
+      // the next segment's query goes into TMEM as soon as this segment's last QK
+      // is done, so the next QKs overlap this segment's last P . C and output
+      const int g_next = tp.tile_start + ie;
+      if (g_next < g1) {
+        const int tn = token_of_tile(a.plan, a.T, g_next);
+        if (tn >= 0 && tn < a.T) {
+          if (!wwait(&cs->q_empty, si & 1, cs, hdr)) return;
+          load_q(tn);
+          q_ready = true;
+        }
+      }
       if (!wwait(&cs->pv_done[last_c & 1], (last_c >> 1) & 1, cs, hdr)) return;
       tc_fence_after();
       const bool complete = ia == 0 && ie == tp.ntiles;
@@ -678,11 +892,12 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)(k * 2 + slot) * H + row) * L + lat_x0 + col);
+          float4* po = reinterpret_cast<float4*>(a.part_o);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                                 __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+            po[part_index(k, slot, (lat_x0 + col) / 4 + i, row, L, H)] =
+                make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                            __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
         }
       }
       // O has been read: the next segment's first P . C may overwrite it
@@ -716,7 +931,15 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         ++nfix;
         if (cs->fix_last) {
           __threadfence();
-          if (live) merge_split_token(a, t, tp, kf, kl, Qt, rank, row, lat_x0, LC);
+          if (tp.tile_start + ie >= g1) {
+            // This was the partition's last segment: O in TMEM still holds this
+            // CTA's own partial and the stage ring is idle.
+            if (!merge_in_tmem(a, cs, t, tp, k, kf, kl, Qt, rank, row, lat_x0, LC, trow, trow + C::kSCol, lse, inv,
+                               sStage, nmrg))
+              return;
+          } else if (live) {
+            merge_split_token(a, t, tp, kf, kl, Qt, rank, row, lat_x0, LC);
+          }
           if (row == 0) a.counters[2 * t + rank] = 0;
         }
       }
@@ -726,11 +949,14 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   // ------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (CL == 2 && tid == 0) {
-    // every remote store / arrive of this CTA is issued; tell the peer, and wait
-    // (bounded) until the peer says the same before this CTA's memory goes away
-    mbar_arrive_cluster(mapa_shared(smem_u32(&cs->bye), peer));
-    if (!mbar_wait<true>(&cs->bye, 0, kWaitLimitNs)) {
+  if (CL == 2 && tid == 32) {
+    // Tell the peer this CTA is done, and wait (bounded) until the peer says the
+    // same before this CTA's shared memory goes away.  Everything the peer sends
+    // into this CTA (multicast tiles, multicast stage commits) has been awaited on
+    // this CTA's own barriers already, so the signal needs no release ordering (a
+    // release at cluster scope here stalled for tens of microseconds).
+    mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&cs->bye), peer));
+    if (!mbar_poll_cluster(&cs->bye, 0, kWaitLimitNs)) {
       record_timeout(&cs->bye, hdr);
       atomicOr(&hdr->status, kDeviceTimeout);
     }
@@ -785,20 +1011,16 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
   bool ok;
   if (MODE == kLoadFp8) {
     const uint64_t rb = (uint64_t)L + 2 * R;   // bytes per cached row
-    ok = encode_2d(&maps.kv_lat, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv_pool, rb, pool_rows, rb, LC, rows,
+    ok = encode_2d(&maps.kv_lat, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv_pool, rb, pool_rows, rb, C::RW, rows,
                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         encode_2d(&maps.kv_rope, kBF16, a.kv_pool, rb / 2, pool_rows, rb, 32, rows, CU_TENSOR_MAP_SWIZZLE_64B);
+         encode_2d(&maps.kv_rope, kBF16, a.kv_pool, rb / 2, pool_rows, rb, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
   } else {
     ok = encode_2d(&maps.kv_lat, kBF16, a.kv_pool, KQ, pool_rows, (uint64_t)KQ * 2, 64, rows,
-                   CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_2d(&maps.kv_rope, kBF16, a.kv_pool, KQ, pool_rows, (uint64_t)KQ * 2, 32, rows,
-                   CU_TENSOR_MAP_SWIZZLE_64B);
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    maps.kv_rope = maps.kv_lat;   // the rope box is one more 64-column box of the same rows
   }
-  ok = ok &&
-       encode_2d(&maps.q_lat, kBF16, a.q_full, KQ, (uint64_t)a.T * kMaxHeads, (uint64_t)KQ * 2, 64, 128,
-                 CU_TENSOR_MAP_SWIZZLE_128B) &&
-       encode_2d(&maps.q_rope, kBF16, a.q_full, KQ, (uint64_t)a.T * kMaxHeads, (uint64_t)KQ * 2, 32, 128,
-                 CU_TENSOR_MAP_SWIZZLE_64B);
+  ok = ok && encode_2d(&maps.q, kBF16, a.q_full, KQ, (uint64_t)a.T * kMaxHeads, (uint64_t)KQ * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<LC, CL, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
@@ -829,10 +1051,13 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t s) {
 }  // namespace tc
 
 // Shapes with a tensor-core instance: (L, R) = (512, 64) on a 2-CTA cluster,
-// and L = 64 with R <= 32 on one CTA; dense pages of 8..64 tokens or a
-// multiple of 64.
+// and L = 64 with R <= 32 on one CTA; qk_nope a multiple of 8, v_head <= 512;
+// dense pages of 8..64 tokens or a multiple of 64.
 bool decode_tc_supported(const mla_dims_t& d) {
   const int ps = d.page_size;
+  // the weight GEMMs read q and w_uk rows through TMA (16-byte row pitch) and
+  // hold at most four 128-row weight blocks of w_uv per CTA
+  if (d.qk_nope % 8 != 0 || d.v_head < 1 || d.v_head > 512) return false;
   if (!(ps % kTileKeys == 0 || (kTileKeys % ps == 0 && ps >= 8))) return false;
   if (d.kv_lora_rank == 512 && d.qk_rope == 64) return true;
   if (d.kv_lora_rank == 64 && d.qk_rope <= 32 && d.qk_rope % 8 == 0) return true;

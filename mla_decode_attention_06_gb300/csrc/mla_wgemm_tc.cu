@@ -9,10 +9,14 @@
 //                   m block also copy q_rope into q_full[t, h, L:L+R].
 //   W_uv   (K3): W = w_uv, m = v column, k = latent column, X = o_lat
 //                -> written as bf16 into out[t, h, v] (and lse copied out).
-// One CTA owns 128 rows m of one head and up to 128 tokens: M = 128 (weight
-// rows), N = tokens, K streamed in 64-column boxes through a 4-deep TMA ring.
-// The weights are read once per token tile, which is what bounds these
-// kernels (HBM): 16.8 MB per weight at the DeepSeek-V3 shapes.
+// One CTA owns one head and up to 128 tokens: all M rows of the head's weight
+// (MB blocks of 128, M <= 512), N = tokens, K streamed in 64-column steps.  A
+// step loads the MB weight boxes and one activation box; the ring is as deep
+// as shared memory allows (the absorb holds all of K = 128, W_uv all of
+// K = 512 in 8 stages), so every load of the CTA is in flight at once and one
+// wave of CTAs (one per head) covers the GEMM.  The weights are read once per
+// token block, which is what bounds these kernels (HBM): 16.8 MB per weight at
+// the DeepSeek-V3 shapes.
 //
 // FP8 weights: e4m3 codes are widened to bf16 (exactly: every e4m3 value is a
 // bf16 value) in shared memory, and the 128 x 128 block scale is applied in
@@ -29,8 +33,10 @@ namespace wg {
 using namespace sm100;
 
 constexpr int kThreads = 128;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;
+constexpr int kMaxMB = 4;                  // 128-row weight blocks per CTA (M <= 512)
 constexpr int kMaxTokens = 128;            // tokens per CTA (MMA N)
+constexpr int kStageBudget = 220 * 1024;   // shared memory for the ring
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int kABytes = 128 * 128;         // 128 rows x 64 bf16
 constexpr int kA8Bytes = 128 * 64;         // 128 rows x 64 e4m3
@@ -44,6 +50,7 @@ struct Args {
   int mode;            // 0 absorb, 1 W_uv
   int H, T, M, K;      // heads, tokens, weight rows per head, contraction length
   int TN;              // tokens per CTA (multiple of 16, <= 128)
+  int MB, S;           // weight row blocks per CTA, ring stages
   const float* wscale; // e4m3 block scales [H, ceil(M/128), ceil(K/128)]
   // absorb
   __nv_bfloat16* q_full; int KQ, L, R, N; const __nv_bfloat16* q;
@@ -71,29 +78,31 @@ template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constant__ Maps maps, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  const int TN = a.TN;
+  const int TN = a.TN, MB = a.MB, S = a.S;
   const int kBBytes = TN * 128;
-  uint8_t* sA = sm;                                  // kStages x [128 x 64] bf16
-  uint8_t* sB = sA + kStages * kABytes;              // kStages x [TN x 64] bf16
-  uint8_t* sA8 = sB + kStages * kBBytes;             // kStages x [128 x 64] e4m3 (fp8 only)
-  uint64_t* full = reinterpret_cast<uint64_t*>(sA8 + (kFp8 ? kStages * kA8Bytes : 0));
-  uint64_t* empty = full + kStages;
-  uint64_t* done = empty + kStages;
+  // stage: MB bf16 weight boxes | activation box | (e4m3) MB raw weight boxes
+  const int stage_smem = MB * kABytes + kBBytes + (kFp8 ? MB * kA8Bytes : 0);
+  const uint32_t stage_tx = MB * (kFp8 ? kA8Bytes : kABytes) + kBBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S * stage_smem);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* done = empty + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  auto w_box = [&](int s, int i) { return sm + s * stage_smem + i * kABytes; };
+  auto x_box = [&](int s) { return sm + s * stage_smem + MB * kABytes; };
+  auto w8_box = [&](int s, int i) { return sm + s * stage_smem + MB * kABytes + kBBytes + i * kA8Bytes; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mb = blockIdx.x, h = blockIdx.y, t0 = blockIdx.z * TN;
+  const int h = blockIdx.y, t0 = blockIdx.z * TN;
   // absorb: the first block also plans the call (first, so it overlaps the other blocks' GEMMs)
-  if (a.mode == 0 && mb == 0 && h == 0 && blockIdx.z == 0) plan_block(a.pin);
-  const int m0 = mb * 128;
-  const int nkb = (a.K + 63) / 64;                 // 64-wide k boxes
-  const int nkb128 = kFp8 ? (a.K + 127) / 128 : 1; // accumulators
-  const int ncols_needed = nkb128 * TN;
+  if (a.mode == 0 && h == 0 && blockIdx.z == 0) plan_block(a.pin);
+  const int nkb = (a.K + 63) / 64;                 // 64-wide k steps
+  const int nacc = kFp8 ? (a.K + 127) / 128 : 1;   // accumulators per weight block
+  const int ncols_needed = MB * nacc * TN;
   const uint32_t tcols = ncols_needed <= 32 ? 32 : ncols_needed <= 64 ? 64 : ncols_needed <= 128 ? 128
                          : ncols_needed <= 256 ? 256 : 512;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -110,59 +119,55 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t stage_bytes = (kFp8 ? kA8Bytes : kABytes) + kBBytes;
 
   auto load_w = [&](int kb) {
-    const int s = kb % kStages;
-    if (kFp8) tma_load_2d(sA8 + s * kA8Bytes, &maps.w, &full[s], kb * 64, h * a.M + m0);
-    else tma_load_2d(sA + s * kABytes, &maps.w, &full[s], kb * 64, h * a.M + m0);
+    const int s = kb % S;
+    for (int i = 0; i < MB; ++i)
+      tma_load_2d(kFp8 ? w8_box(s, i) : w_box(s, i), &maps.w, &full[s], kb * 64, h * a.M + 128 * i);
   };
   auto load_x = [&](int kb) {
-    const int s = kb % kStages;
+    const int s = kb % S;
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-            smem_u32(sB + s * kBBytes)),
+            smem_u32(x_box(s))),
         "l"(reinterpret_cast<uint64_t>(&maps.x)), "r"(smem_u32(&full[s])), "r"(kb * 64), "r"(h), "r"(t0)
         : "memory");
   };
-  auto load = [&](int kb) {
-    mbar_arrive_expect_tx(&full[kb % kStages], stage_bytes);
-    load_w(kb);
-    load_x(kb);
-  };
   // weights do not depend on the previous kernel: start streaming them first
   if (tid == 0)
-    for (int kb = 0; kb < nkb && kb < kStages; ++kb) {
-      mbar_arrive_expect_tx(&full[kb], stage_bytes);
+    for (int kb = 0; kb < nkb && kb < S; ++kb) {
+      mbar_arrive_expect_tx(&full[kb], stage_tx);
       load_w(kb);
     }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // o_lat / lse of the decode (W_uv)
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // q (absorb) / o_lat, lse of the decode (W_uv)
   if (tid == 0)
-    for (int kb = 0; kb < nkb && kb < kStages; ++kb) load_x(kb);
+    for (int kb = 0; kb < nkb && kb < S; ++kb) load_x(kb);
 
   const uint32_t idesc = idesc_bf16_f32(128, TN, false, false);
   bool ok = true;
   for (int kb = 0; kb < nkb; ++kb) {
-    const int s = kb % kStages;
+    const int s = kb % S;
     // every thread waits; the CTA proceeds only if all saw the stage arrive
-    if (!__syncthreads_and(wait_bar(&full[s], (kb / kStages) & 1, a.hdr))) {
+    if (!__syncthreads_and(wait_bar(&full[s], (kb / S) & 1, a.hdr))) {
       ok = false;
       break;
     }
     if (kFp8) {
-      // widen row `tid` of the e4m3 box into the 128B-swizzled bf16 layout
-      const uint8_t* src = sA8 + s * kA8Bytes + tid * 64;
-      uint8_t* dst = sA + s * kABytes + tid * 128;
+      // widen row `tid` of each e4m3 box into the 128B-swizzled bf16 layout
+      for (int i = 0; i < MB; ++i) {
+        const uint8_t* src = w8_box(s, i) + tid * 64;
+        uint8_t* dst = w_box(s, i) + tid * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(src + ch * 8);
-        uint4 v;
-        v.x = e4m3x2_to_bf16x2((uint16_t)(raw.x & 0xffff));
-        v.y = e4m3x2_to_bf16x2((uint16_t)(raw.x >> 16));
-        v.z = e4m3x2_to_bf16x2((uint16_t)(raw.y & 0xffff));
-        v.w = e4m3x2_to_bf16x2((uint16_t)(raw.y >> 16));
-        *reinterpret_cast<uint4*>(dst + ((ch ^ (tid & 7)) * 16)) = v;
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(src + ch * 8);
+          uint4 v;
+          v.x = e4m3x2_to_bf16x2((uint16_t)(raw.x & 0xffff));
+          v.y = e4m3x2_to_bf16x2((uint16_t)(raw.x >> 16));
+          v.z = e4m3x2_to_bf16x2((uint16_t)(raw.y & 0xffff));
+          v.w = e4m3x2_to_bf16x2((uint16_t)(raw.y >> 16));
+          *reinterpret_cast<uint4*>(dst + ((ch ^ (tid & 7)) * 16)) = v;
+        }
       }
       fence_proxy_async_smem();
       __syncthreads();
@@ -172,17 +177,23 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     if (tid == 0) {
       const int acc = kFp8 ? (kb >> 1) : 0;
       const bool first_in_acc = kFp8 ? ((kb & 1) == 0) : (kb == 0);
+      const uint64_t bd0 = smem_desc(smem_u32(x_box(s)), 16, 1024, kLayoutSw128);
+      for (int i = 0; i < MB; ++i) {
+        const uint64_t ad0 = smem_desc(smem_u32(w_box(s, i)), 16, 1024, kLayoutSw128);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t ad = smem_desc(smem_u32(sA + s * kABytes) + kk * 32, 16, 1024, kLayoutSw128);
-        const uint64_t bd = smem_desc(smem_u32(sB + s * kBBytes) + kk * 32, 16, 1024, kLayoutSw128);
-        mma_ss(tmem + acc * TN, ad, bd, idesc, (first_in_acc && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem + (i * nacc + acc) * TN, ad0 + (uint64_t)(kk * 2), bd0 + (uint64_t)(kk * 2), idesc,
+                 (first_in_acc && kk == 0) ? 0u : 1u);
       }
       mma_commit(&empty[s]);
-      if (kb + kStages < nkb) {
+      if (kb + S < nkb) {
         // the stage is refilled once the MMAs above have read it
-        issued_ok = wait_bar(&empty[s], (kb / kStages) & 1, a.hdr);
-        if (issued_ok) load(kb + kStages);
+        issued_ok = wait_bar(&empty[s], (kb / S) & 1, a.hdr);
+        if (issued_ok) {
+          mbar_arrive_expect_tx(&full[s], stage_tx);
+          load_w(kb + S);
+          load_x(kb + S);
+        }
       }
     }
     if (!__syncthreads_and(issued_ok)) {
@@ -196,55 +207,79 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   tc_fence_after();
 
   // ------------------------------------------------------------------ epilogue
-  const int row = 32 * warp + lane;    // weight row within the block = TMEM lane
-  const int m = m0 + row;
+  const int row = 32 * warp + lane;    // weight row within a block = TMEM lane
   const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
-  float sc[4] = {1.f, 1.f, 1.f, 1.f};
-  if (kFp8) {
-    const int nmb = (a.M + 127) / 128;
-    for (int b = 0; b < nkb128 && b < 4; ++b) sc[b] = a.wscale[((size_t)h * nmb + mb) * nkb128 + b];
-  }
-  for (int j0 = 0; j0 < TN; j0 += 16) {
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.f;
-    for (int b = 0; b < nkb128; ++b) {
-      uint32_t r[16];
-      tmem_ld16(trow + b * TN + j0, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] += sc[b] * __uint_as_float(r[i]);
+  for (int i = 0; i < MB; ++i) {
+    const int m = 128 * i + row;
+    float sc[4] = {1.f, 1.f, 1.f, 1.f};
+    if (kFp8) {
+      const int nmb = (a.M + 127) / 128;
+      for (int b = 0; b < nacc && b < 4; ++b) sc[b] = a.wscale[((size_t)h * nmb + i) * nacc + b];
     }
-    if (!fin || !ok || m >= a.M) continue;
+    for (int j0 = 0; j0 < TN; j0 += 32) {
+      // 32 token columns of every accumulator in flight before one wait
+      float v[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = t0 + j0 + i;
-      if (t >= a.T) break;
-      if (a.mode == 0)
-        a.q_full[((size_t)t * kMaxHeads + h) * a.KQ + m] = __float2bfloat16_rn(v[i]);
-      else
-        a.out[((size_t)t * a.H + h) * a.V + m] = __float2bfloat16_rn(v[i]);
-    }
-  }
-  if (mb == 0) {
-    if (a.mode == 0) {
-      // rope columns are copied unchanged; absent heads are zero rows
-      for (int i = tid; i < TN * a.R; i += kThreads) {
-        const int t = t0 + i / a.R, r = i % a.R;
-        if (t < a.T)
-          a.q_full[((size_t)t * kMaxHeads + h) * a.KQ + a.L + r] = a.q[((size_t)t * a.H + h) * (a.N + a.R) + a.N + r];
+      for (int q = 0; q < 32; ++q) v[q] = 0.f;
+      for (int b = 0; b < nacc; ++b) {
+        uint32_t r[32];
+        if (j0 + 32 <= TN) {
+          tmem_ld32(trow + (i * nacc + b) * TN + j0, r);
+        } else {
+          tmem_ld16(trow + (i * nacc + b) * TN + j0, *reinterpret_cast<uint32_t(*)[16]>(r));
+#pragma unroll
+          for (int q = 16; q < 32; ++q) r[q] = 0u;
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] += sc[b] * __uint_as_float(r[q]);
       }
-      if (h == 0 && a.H < kMaxHeads) {
-        const int per = (kMaxHeads - a.H) * a.KQ;
-        for (int i = tid; i < TN * per; i += kThreads) {
-          const int t = t0 + i / per;
-          if (t < a.T) a.q_full[((size_t)t * kMaxHeads + a.H) * a.KQ + i % per] = __float2bfloat16_rn(0.f);
+      if (!fin || !ok || m >= a.M) continue;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int t = t0 + j0 + q;
+        if (j0 + q < TN && t < a.T) {
+          if (a.mode == 0)
+            a.q_full[((size_t)t * kMaxHeads + h) * a.KQ + m] = __float2bfloat16_rn(v[q]);
+          else
+            a.out[((size_t)t * a.H + h) * a.V + m] = __float2bfloat16_rn(v[q]);
         }
       }
-    } else if (a.lse_out) {
-      for (int j = tid; j < TN; j += kThreads)
-        if (t0 + j < a.T) a.lse_out[(size_t)(t0 + j) * a.H + h] = a.lse_ws[(size_t)(t0 + j) * a.H + h];
     }
+  }
+  if (a.mode == 0) {
+    // rope columns are copied unchanged, 16 bytes at a time; every load of the
+    // thread is issued before its stores (q and q_full may not alias, but the
+    // compiler cannot know that)
+    {
+      const int cpr = a.R / 8;   // 16-byte chunks per (token, head) row
+      constexpr int kBatch = 8;
+      for (int i0 = tid; i0 < TN * cpr; i0 += kThreads * kBatch) {
+        uint4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int i = i0 + j * kThreads, t = t0 + i / cpr;
+          if (i < TN * cpr && t < a.T)
+            v[j] = __ldg(reinterpret_cast<const uint4*>(a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N) + i % cpr);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const int i = i0 + j * kThreads, t = t0 + i / cpr;
+          if (i < TN * cpr && t < a.T)
+            reinterpret_cast<uint4*>(a.q_full + ((size_t)t * kMaxHeads + h) * a.KQ + a.L)[i % cpr] = v[j];
+        }
+      }
+    }
+    if (h == 0 && a.H < kMaxHeads) {
+      const int per = (kMaxHeads - a.H) * a.KQ;
+      for (int i = tid; i < TN * per; i += kThreads) {
+        const int t = t0 + i / per;
+        if (t < a.T) a.q_full[((size_t)t * kMaxHeads + a.H) * a.KQ + i % per] = __float2bfloat16_rn(0.f);
+      }
+    }
+  } else if (a.lse_out) {
+    for (int j = tid; j < TN; j += kThreads)
+      if (t0 + j < a.T) a.lse_out[(size_t)(t0 + j) * a.H + h] = a.lse_ws[(size_t)(t0 + j) * a.H + h];
   }
   tc_fence_before();
   __syncthreads();
@@ -277,6 +312,22 @@ cudaError_t launch(const Args& a0, WFmt wf, const void* w, const void* x, int Kx
   EncodeTiledFn fn = encode_fn();
   if (!fn || a.T == 0) return a.T == 0 ? cudaSuccess : cudaErrorInvalidValue;
   a.TN = a.T >= kMaxTokens ? kMaxTokens : ((a.T + 15) / 16) * 16;
+  a.MB = (a.M + 127) / 128;
+  if (a.MB > kMaxMB) return cudaErrorInvalidValue;
+  {
+    // TMEM: MB weight blocks x (e4m3: one accumulator per 128-wide k block) x TN columns
+    const int nacc = wf == WFmt::kE4M3 ? (a.K + 127) / 128 : 1;
+    while (a.TN > 16 && a.MB * nacc * a.TN > 512) a.TN -= 16;
+    if (a.MB * nacc * a.TN > 512) return cudaErrorInvalidValue;
+  }
+  const int stage_smem = a.MB * kABytes + a.TN * 128 + (wf == WFmt::kE4M3 ? a.MB * kA8Bytes : 0);
+  {
+    const int nkb = (a.K + 63) / 64;
+    int st = kStageBudget / stage_smem;
+    if (st > kMaxStages) st = kMaxStages;
+    if (st > nkb) st = nkb;
+    a.S = st < 1 ? 1 : st;
+  }
   Maps maps;
   {
     const bool f8 = wf == WFmt::kE4M3;
@@ -301,8 +352,8 @@ cudaError_t launch(const Args& a0, WFmt wf, const void* w, const void* x, int Kx
       return cudaErrorInvalidValue;
   }
   const bool f8 = wf == WFmt::kE4M3;
-  const size_t smem = 1024 + kStages * (kABytes + a.TN * 128) + (f8 ? kStages * kA8Bytes : 0) + 256;
-  dim3 grid((a.M + 127) / 128, a.H, (a.T + a.TN - 1) / a.TN);
+  const size_t smem = 1024 + (size_t)a.S * stage_smem + (2 * kMaxStages + 2) * 8;
+  dim3 grid(1, a.H, (a.T + a.TN - 1) / a.TN);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
