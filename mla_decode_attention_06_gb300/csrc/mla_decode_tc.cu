@@ -183,10 +183,10 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint16_t two, float sca
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// Two floats rounded to a bf16 pair (low half = lo) in one conversion.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return a | (b << 16);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -537,12 +537,12 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           // pages of this tile that hold at least one live row; both CTAs count the
           // same bytes, half of which the peer's multicast delivers
           const uint32_t row_bytes = (MODE == kLoadFp8 ? L : C::NLB * 128) + 128;
+          uint32_t live_rows = 0;
+          for (int p = 0; p < nloads; ++p)
+            if ((mask >> (p * rows_per_load)) & lmask) live_rows += rows_per_load;
           if (lane == 0) {
             cs->row_mask[s] = mask;
-            uint32_t bytes = 0;
-            for (int p = 0; p < nloads; ++p)
-              if ((mask >> (p * rows_per_load)) & lmask) bytes += rows_per_load * row_bytes;
-            mbar_arrive_expect_tx(&cs->kv_full[s], bytes);
+            mbar_arrive_expect_tx(&cs->kv_full[s], live_rows * row_bytes);
           }
           __syncwarp();
           for (int p = 0; p < nloads; ++p) {
@@ -608,8 +608,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       for (int it = ia; it < ie; ++it, ++cq) {
         if (waborted(cs)) return;
         const int s = cq % S, b = cq & 1;
-        if (!wwait(MODE == kLoadFp8 ? &cs->kv_conv[s] : &cs->kv_full[s], (cq / S) & 1, cs, hdr)) return;
+        const uint32_t par = (cq / S) & 1;
         if (cq >= 2 && !wwait(&cs->pv_done[b], ((cq - 2) >> 1) & 1, cs, hdr)) return;
+        if (!wwait(MODE == kLoadFp8 ? &cs->kv_conv[s] : &cs->kv_full[s], par, cs, hdr)) return;
         const uint64_t mask = cs->row_mask[s];
         if (MODE != kLoadFp8 && mask != ~0ull) {
           // Rows outside the key range may hold anything (NaN included).  Their
@@ -629,23 +630,33 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           __syncwarp();
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint64_t dk = dk0 + (uint64_t)((s * C::kStageBytes) >> 4);
-          const uint32_t sd = tmem + C::kSCol + 64 * b;
-          // latent [0, QT): A = query in TMEM
+        const uint64_t dk = dk0 + (uint64_t)((s * C::kStageBytes) >> 4);
+        const uint32_t sd = tmem + C::kSCol + 64 * b;
+        // latent [0, QT): A = query in TMEM; the MMA queue is shallow, so the
+        // issue runs back to back
 #pragma unroll
-          for (int kk = 0; kk < C::QT / 16; ++kk)
-            mma_ts(sd, tmem + C::kQCol + 8 * kk, dk + (uint64_t)(((kk >> 2) * C::kBox + (kk & 3) * 32) >> 4),
-                   idesc_qk, kk > 0 ? 1u : 0u);
-          // latent [QT, L): A = query boxes in shared memory
+        for (int j = 0; j < C::QT / 64; ++j) {
+          if (lane == 0) {
 #pragma unroll
-          for (int i = 0; i < C::NQS; ++i) {
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(sd, tmem + C::kQCol + 8 * (4 * j + kk), dk + (uint64_t)((j * C::kBox + kk * 32) >> 4), idesc_qk,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          __syncwarp();
+        }
+        // latent [QT, L): A = query boxes in shared memory
+#pragma unroll
+        for (int i = 0; i < C::NQS; ++i) {
+          if (lane == 0) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(sd, dq0 + (uint64_t)((i * C::kQBox + kk * 32) >> 4),
                      dk + (uint64_t)(((C::QT / 64 + i) * C::kBox + kk * 32) >> 4), idesc_qk, 1u);
           }
-          // rope (64 columns; past qk_rope both sides read the TMA zero fill)
+          __syncwarp();
+        }
+        // rope (64 columns; past qk_rope both sides read the TMA zero fill)
+        if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ss(sd, dq0 + (uint64_t)((C::NQS * C::kQBox + kk * 32) >> 4),
@@ -796,19 +807,39 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         float sv[64];
 #pragma unroll
         for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(sr[j]);
-        // row max of the scaled scores (log2 domain); dead keys do not count
+        // row max of the scaled scores (log2 domain); dead keys do not count.
+        // Eight independent chains, then a tree, keep the dependency depth short;
+        // full tiles (the common case) skip the mask tests.
         const bool all_live = mask == ~0ull;
         float mx;
-        if (sl2 >= 0.f) {
-          float r = -CUDART_INF_F;
+        {
+          const bool up = sl2 >= 0.f;   // the max of s * scale is the min of s when scale < 0
+          float r8[8];
 #pragma unroll
-          for (int j = 0; j < 64; ++j) r = fmaxf(r, (all_live || ((mask >> j) & 1ull)) ? sv[j] : -CUDART_INF_F);
-          mx = r == -CUDART_INF_F ? r : r * sl2;
-        } else {
-          float r = CUDART_INF_F;
+          for (int i = 0; i < 8; ++i) r8[i] = sv[i];
+          if (all_live) {
+            if (up) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) r = fminf(r, (all_live || ((mask >> j) & 1ull)) ? sv[j] : CUDART_INF_F);
-          mx = r == CUDART_INF_F ? -CUDART_INF_F : r * sl2;
+              for (int j = 8; j < 64; ++j) r8[j & 7] = fmaxf(r8[j & 7], sv[j]);
+            } else {
+#pragma unroll
+              for (int j = 8; j < 64; ++j) r8[j & 7] = fminf(r8[j & 7], sv[j]);
+            }
+          } else {
+            const float fill = up ? -CUDART_INF_F : CUDART_INF_F;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) r8[i] = ((mask >> i) & 1ull) ? sv[i] : fill;
+#pragma unroll
+            for (int j = 8; j < 64; ++j) {
+              const float x = ((mask >> j) & 1ull) ? sv[j] : fill;
+              r8[j & 7] = up ? fmaxf(r8[j & 7], x) : fminf(r8[j & 7], x);
+            }
+          }
+#pragma unroll
+          for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) r8[i] = up ? fmaxf(r8[i], r8[i + w]) : fminf(r8[i], r8[i + w]);
+          mx = r8[0] == (up ? -CUDART_INF_F : CUDART_INF_F) ? -CUDART_INF_F : r8[0] * sl2;
         }
         // Lazy rescale: a row moves its reference max only when the new max is
         // more than 2^8 above it.  tcgen05.ld/st are warp-collective, so when any
@@ -837,20 +868,28 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (m == -CUDART_INF_F) m = mx;   // first live key of the segment: O is still empty
         // P = 2^(scale * log2(e) * s - m) as bf16 pairs over the S columns in TMEM
         uint32_t pk[32];
-        float psum = 0.f;
+        float ps4[4] = {0.f, 0.f, 0.f, 0.f};
         const float neg_m = -m;
+        if (all_live) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float p0 = ex2(fmaf(sv[2 * j], sl2, neg_m));
-          float p1 = ex2(fmaf(sv[2 * j + 1], sl2, neg_m));
-          if (!all_live) {
+          for (int j = 0; j < 32; ++j) {
+            const float p0 = ex2(fmaf(sv[2 * j], sl2, neg_m));
+            const float p1 = ex2(fmaf(sv[2 * j + 1], sl2, neg_m));
+            ps4[j & 3] += p0 + p1;
+            pk[j] = pack_bf16(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float p0 = ex2(fmaf(sv[2 * j], sl2, neg_m));
+            float p1 = ex2(fmaf(sv[2 * j + 1], sl2, neg_m));
             p0 = ((mask >> (2 * j)) & 1ull) ? p0 : 0.f;
             p1 = ((mask >> (2 * j + 1)) & 1ull) ? p1 : 0.f;
+            ps4[j & 3] += p0 + p1;
+            pk[j] = pack_bf16(p0, p1);
           }
-          psum += p0 + p1;
-          pk[j] = pack_bf16(p0, p1);
         }
-        l += psum;
+        l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         tmem_st32(trow + C::kSCol + 64 * b, pk);
         tmem_st_wait();
         tc_fence_before();

@@ -116,6 +116,17 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t p
   return ok != 0;
 }
 
+// Spins (never suspends) on a phase that is expected within a microsecond or
+// so; false after `limit_ns`.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 15u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Polls (never suspends) for a phase that another CTA of the cluster
 // completes, backing off with short sleeps; false after `limit_ns`.
 __device__ __forceinline__ bool mbar_poll_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
