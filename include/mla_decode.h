@@ -57,7 +57,7 @@ typedef enum {
   MLA_ERR_INVALID_ARG = 1,        /* NULL required pointer, bad sizes, bad mask or window */
   MLA_ERR_UNSUPPORTED = 2,        /* shape without a kernel instance, H > 128, q_scale != NULL;
                                      instances: (L, R) = (512, 64), or L = 64 with R <= 32 (R % 8 == 0);
-                                     N % 8 == 0; V <= 512;
+                                     N % 8 == 0; V % 8 == 0, V <= 512;
                                      page_size in {8, 16, 32, 64} or a multiple of 64 */
   MLA_ERR_WORKSPACE_TOO_SMALL = 3,
   MLA_ERR_CUDA = 4,               /* a CUDA runtime or driver call failed */

@@ -67,6 +67,7 @@ struct Smem {   // control block after the stage ring
   uint64_t kv_conv[kMaxStages];  // e4m3 rows widened (kLoadFp8)
   uint64_t row_mask[kMaxStages];
   uint64_t q_full, q_empty;
+  uint64_t qa_full, qa_done;     // query latent [0, QT) staged in shared memory / moved into TMEM
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_free;
   uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
@@ -105,6 +106,7 @@ struct Cfg {
   static_assert(LC % 64 == 0 && (CL == 1 || CL == 2), "latent slice");
   static_assert(kQCol + QT / 2 <= 512, "TMEM columns");
   static_assert(NRH % CL == 0, "raw boxes split over the cluster");
+  static_assert(QT / 64 <= NQS + 1, "the query staging fits the query buffer");
   static_assert(kSmem <= 232448, "shared memory");
 };
 
@@ -114,26 +116,36 @@ struct Maps {
   CUtensorMap q;         // absorbed queries [T * 128, L + R], 64-column boxes
 };
 
-// Walks the segments of partition k: calls f(t, plan, first_tile, end_tile, g_first).
+// Walks the segments of partition k: calls f(si, t, plan, first_tile, end_tile,
+// is_first_segment, next_t) where next_t is the token of the following segment
+// (-1 if none).  Consecutive segments belong to consecutive tokens, so the plan
+// entry of token t + 1 is loaded when segment t starts and is ready at the
+// boundary; only a token without keys in between (they share tile_start) falls
+// back to the search.
 template <class F>
 __device__ __forceinline__ void for_each_segment(const DecodeArgs& a, int g0, int g1, F&& f) {
   int g = g0;
   int si = 0;
+  int t = g0 < g1 ? token_of_tile(a.plan, a.T, g0) : 0;
   while (g < g1) {
-    const int t = token_of_tile(a.plan, a.T, g);
     if (t < 0 || t >= a.T) {   // a plan that does not cover g: report, never loop
       atomicOr(&a.hdr_mut->status, kDeviceCheckFailed);
       return;
     }
     const TokenPlan tp = a.plan[t];
+    const TokenPlan tn = t + 1 < a.T ? a.plan[t + 1] : TokenPlan{};
     const int ia = g - tp.tile_start;
     const int ie = min(g1, tp.tile_start + tp.ntiles) - tp.tile_start;
     if (ia < 0 || ie <= ia) {
       atomicOr(&a.hdr_mut->status, kDeviceCheckFailed);
       return;
     }
-    f(si, t, tp, ia, ie, g == g0);
-    g = tp.tile_start + ie;
+    const int g_next = tp.tile_start + ie;
+    int next_t = -1;
+    if (g_next < g1) next_t = (t + 1 < a.T && tn.ntiles > 0) ? t + 1 : token_of_tile(a.plan, a.T, g_next);
+    f(si, t, tp, ia, ie, g == g0, next_t);
+    g = g_next;
+    t = next_t;
     ++si;
   }
 }
@@ -390,6 +402,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     }
     mbar_init(&cs->q_full, 1 + 128);     // producer (TMA bytes) + every softmax thread (TMEM part)
     mbar_init(&cs->q_empty, 1);
+    mbar_init(&cs->qa_full, 1);
+    mbar_init(&cs->qa_done, 128);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&cs->s_full[b], 1);
       mbar_init(&cs->p_full[b], 128);
@@ -437,8 +451,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     };
     int c = 0;
     bool bad = false;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
+    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int next_t) {
       bool q_pending = true;   // the query's shared-memory part goes right after the first tile
+      // The next segment's absorbed query is read at this segment's end; it goes
+      // into L2 a few tiles before that (earlier, the cache stream evicts it again).
+      const int q_prefetch_at = ie - 4 > ia ? ie - 4 : ia;
       constexpr int kOwn = MODE == kLoadFp8 ? C::NRH / CL : C::NLB / CL;   // this CTA's boxes per load
       const int nloads = kTileKeys / rows_per_load;
       const uint64_t lmask = rows_per_load == 64 ? ~0ull : ((1ull << rows_per_load) - 1);
@@ -503,6 +520,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
         const int s = c % S;
+        if (lane == 0 && it == q_prefetch_at && next_t >= 0 && next_t < a.T)
+          bulk_prefetch_l2(a.q_full + (size_t)next_t * kMaxHeads * KQ, (uint32_t)(kMaxHeads * KQ * 2));
         // global reads, issued before the wait for the stage so their latency overlaps it
         bool v[2];
         int rid[2], pg[2];
@@ -567,8 +586,18 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         }
         __syncwarp();
         if (q_pending) {
-          // the previous segment's last QK has read the query buffers
+          // The previous segment's last QK has read the query buffers.  The query's
+          // TMEM part (latent [0, QT)) comes in through the shared-memory buffer
+          // first: TMA, then the softmax threads copy their rows into TMEM; then
+          // the buffer takes the shared-memory part (latent [QT, L) and rope).
           if (si > 0 && !wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&cs->qa_full, (C::QT / 64) * C::kQBox);
+            for (int i = 0; i < C::QT / 64; ++i)
+              tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->qa_full, 64 * i, t * kMaxHeads);
+          }
+          __syncwarp();
+          if (!wwait(&cs->qa_done, si & 1, cs, hdr)) return;
           if (lane == 0) {
             mbar_arrive_expect_tx(&cs->q_full, C::kQBytes);
             for (int i = 0; i < C::NQS; ++i)
@@ -601,7 +630,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSw128);
     const uint64_t dk0 = smem_desc(smem_u32(sStage), 16, 1024, kLayoutSw128);
     int cq = 0, nseg = 0;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
+    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       nseg = si + 1;
       if (waborted(cs)) return;
       if (!wwait(&cs->q_full, si & 1, cs, hdr)) return;
@@ -679,7 +708,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const uint32_t idesc_pv = idesc_bf16_f32(128, LC, false, true);
     const uint64_t dv0 = smem_desc(smem_u32(sStage) + (lat_x0 / 64) * C::kBox, C::kBox, 1024, kLayoutSw128);
     int cp = 0;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
+    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++cp) {
         if (waborted(cs)) return;
         const int b = cp & 1;
@@ -709,7 +738,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     // writes those boxes.
     const int ci = tid - 192;
     int c = 0;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool) {
+    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
         const int s = c % S;
@@ -758,37 +787,39 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const int row = 32 * q + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
     const float sl2 = a.scale * 1.4426950408889634f;
-    // this head's absorbed query, latent [0, QT), into TMEM as bf16 pairs (low half = even column)
-    auto load_q = [&](int t) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.q_full + ((size_t)t * kMaxHeads + row) * KQ);
-      const bool has = row < H;
+    // segment si's query, latent [0, QT), from the staging buffer (128 rows x 128 B
+    // per 64 columns, 128B-swizzled) into this head's TMEM row as bf16 pairs
+    // (low half = even column); then the buffer is released to the producer
+    auto copy_q = [&](int si_q) -> bool {
+      if (!wwait(&cs->qa_full, si_q & 1, cs, hdr)) return false;
 #pragma unroll 1
-      for (int w0 = 0; w0 < C::QT / 2; w0 += 32) {
+      for (int i = 0; i < C::QT / 64; ++i) {
+        const uint8_t* rowp = sQ + i * C::kQBox + row * 128;
         uint32_t w[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = has ? __ldcg(src + w0 / 4 + i) : make_uint4(0, 0, 0, 0);
-          w[4 * i] = v.x;
-          w[4 * i + 1] = v.y;
-          w[4 * i + 2] = v.z;
-          w[4 * i + 3] = v.w;
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((ch ^ (row & 7)) << 4));
+          w[4 * ch] = v.x;
+          w[4 * ch + 1] = v.y;
+          w[4 * ch + 2] = v.z;
+          w[4 * ch + 3] = v.w;
         }
-        tmem_st32(trow + C::kQCol + w0, w);
+        tmem_st32(trow + C::kQCol + 32 * i, w);
       }
       tmem_st_wait();
       tc_fence_before();
+      mbar_arrive(&cs->qa_done);
       mbar_arrive(&cs->q_full);
+      return true;
     };
     int c = 0;
     int nfix = 0;   // split-token merges attempted (phase of fix_bar / fix_done)
     int nmrg = 0;   // partials brought in by bulk copy (phase of mrg_full / mrg_done)
     bool q_ready = false;   // the coming segment's query is already in TMEM
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg) {
+    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
+                                     int next_t) {
       if (waborted(cs)) return;
-      if (!q_ready) {
-        if (si > 0 && !wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
-        load_q(t);
-      }
+      if (!q_ready && !copy_q(si)) return;
       q_ready = false;
       float m = -CUDART_INF_F, l = 0.f;
       int last_c = -1;
@@ -900,14 +931,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       // ------------------------------------------------------------- epilogue
       // the next segment's query goes into TMEM as soon as this segment's last QK
       // is done, so the next QKs overlap this segment's last P . C and output
-      const int g_next = tp.tile_start + ie;
-      if (g_next < g1) {
-        const int tn = token_of_tile(a.plan, a.T, g_next);
-        if (tn >= 0 && tn < a.T) {
-          if (!wwait(&cs->q_empty, si & 1, cs, hdr)) return;
-          load_q(tn);
-          q_ready = true;
-        }
+      if (next_t >= 0 && next_t < a.T) {
+        if (!copy_q(si + 1)) return;
+        q_ready = true;
       }
       if (!wwait(&cs->pv_done[last_c & 1], (last_c >> 1) & 1, cs, hdr)) return;
       tc_fence_after();
@@ -1090,13 +1116,14 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t s) {
 }  // namespace tc
 
 // Shapes with a tensor-core instance: (L, R) = (512, 64) on a 2-CTA cluster,
-// and L = 64 with R <= 32 on one CTA; qk_nope a multiple of 8, v_head <= 512;
+// and L = 64 with R <= 32 on one CTA; qk_nope and v_head multiples of 8, v_head <= 512;
 // dense pages of 8..64 tokens or a multiple of 64.
 bool decode_tc_supported(const mla_dims_t& d) {
   const int ps = d.page_size;
-  // the weight GEMMs read q and w_uk rows through TMA (16-byte row pitch) and
-  // hold at most four 128-row weight blocks of w_uv per CTA
-  if (d.qk_nope % 8 != 0 || d.v_head < 1 || d.v_head > 512) return false;
+  // the weight GEMMs read q and w_uk rows through TMA (16-byte row pitch),
+  // write 16-byte pieces of the output rows, and hold at most four 128-row
+  // weight blocks of w_uv per CTA
+  if (d.qk_nope % 8 != 0 || d.v_head < 8 || d.v_head > 512 || d.v_head % 8 != 0) return false;
   if (!(ps % kTileKeys == 0 || (kTileKeys % ps == 0 && ps >= 8))) return false;
   if (d.kv_lora_rank == 512 && d.qk_rope == 64) return true;
   if (d.kv_lora_rank == 64 && d.qk_rope <= 32 && d.qk_rope % 8 == 0) return true;

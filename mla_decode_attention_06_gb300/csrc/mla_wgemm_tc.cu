@@ -23,6 +23,8 @@
 // the epilogue; because the scale changes every 128 columns of k, each
 // 128-wide k block accumulates into its own TMEM columns and the epilogue sums
 // scale_b * D_b.
+#include <algorithm>
+
 #include "mla_kernels.cuh"
 #include "mla_plan.cuh"
 #include "sm100_ptx.cuh"
@@ -83,7 +85,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   // stage: MB bf16 weight boxes | activation box | (e4m3) MB raw weight boxes
   const int stage_smem = MB * kABytes + kBBytes + (kFp8 ? MB * kA8Bytes : 0);
   const uint32_t stage_tx = MB * (kFp8 ? kA8Bytes : kABytes) + kBBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + S * stage_smem);
+  // the ring, reused by the epilogue as a [MB][TN][128] bf16 staging tile
+  const int ring_bytes = max(S * stage_smem, MB * TN * 128 * 2);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + ring_bytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -145,15 +149,48 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     for (int kb = 0; kb < nkb && kb < S; ++kb) load_x(kb);
 
   const uint32_t idesc = idesc_bf16_f32(128, TN, false, false);
-  bool ok = true;
-  for (int kb = 0; kb < nkb; ++kb) {
-    const int s = kb % S;
-    // every thread waits; the CTA proceeds only if all saw the stage arrive
-    if (!__syncthreads_and(wait_bar(&full[s], (kb / S) & 1, a.hdr))) {
-      ok = false;
-      break;
+  // MMAs of k step kb (stage s) into the accumulators, and the stage's refill
+  auto issue = [&](int kb, int s) -> bool {
+    const int acc = kFp8 ? (kb >> 1) : 0;
+    const bool first_in_acc = kFp8 ? ((kb & 1) == 0) : (kb == 0);
+    const uint64_t bd0 = smem_desc(smem_u32(x_box(s)), 16, 1024, kLayoutSw128);
+    for (int i = 0; i < MB; ++i) {
+      const uint64_t ad0 = smem_desc(smem_u32(w_box(s, i)), 16, 1024, kLayoutSw128);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tmem + (i * nacc + acc) * TN, ad0 + (uint64_t)(kk * 2), bd0 + (uint64_t)(kk * 2), idesc,
+               (first_in_acc && kk == 0) ? 0u : 1u);
     }
-    if (kFp8) {
+    mma_commit(&empty[s]);
+    if (kb + S < nkb) {
+      // the stage is refilled once the MMAs above have read it
+      if (!wait_bar(&empty[s], (kb / S) & 1, a.hdr)) return false;
+      mbar_arrive_expect_tx(&full[s], stage_tx);
+      load_w(kb + S);
+      load_x(kb + S);
+    }
+    return true;
+  };
+  bool ok = true;
+  if (!kFp8) {
+    // one thread runs the whole k loop; the others only wait for the result
+    if (tid == 0) {
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int s = kb % S;
+        ok = wait_bar(&full[s], (kb / S) & 1, a.hdr);
+        if (!ok) break;
+        tc_fence_after();
+        ok = issue(kb, s);
+      }
+    }
+  } else {
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % S;
+      // every thread waits; the CTA proceeds only if all saw the stage arrive
+      if (!__syncthreads_and(wait_bar(&full[s], (kb / S) & 1, a.hdr))) {
+        ok = false;
+        break;
+      }
       // widen row `tid` of each e4m3 box into the 128B-swizzled bf16 layout
       for (int i = 0; i < MB; ++i) {
         const uint8_t* src = w8_box(s, i) + tid * 64;
@@ -171,46 +208,29 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
       }
       fence_proxy_async_smem();
       __syncthreads();
-    }
-    tc_fence_after();
-    bool issued_ok = true;
-    if (tid == 0) {
-      const int acc = kFp8 ? (kb >> 1) : 0;
-      const bool first_in_acc = kFp8 ? ((kb & 1) == 0) : (kb == 0);
-      const uint64_t bd0 = smem_desc(smem_u32(x_box(s)), 16, 1024, kLayoutSw128);
-      for (int i = 0; i < MB; ++i) {
-        const uint64_t ad0 = smem_desc(smem_u32(w_box(s, i)), 16, 1024, kLayoutSw128);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + (i * nacc + acc) * TN, ad0 + (uint64_t)(kk * 2), bd0 + (uint64_t)(kk * 2), idesc,
-                 (first_in_acc && kk == 0) ? 0u : 1u);
+      tc_fence_after();
+      bool issued_ok = true;
+      if (tid == 0) issued_ok = issue(kb, s);
+      if (!__syncthreads_and(issued_ok)) {
+        ok = false;
+        break;
       }
-      mma_commit(&empty[s]);
-      if (kb + S < nkb) {
-        // the stage is refilled once the MMAs above have read it
-        issued_ok = wait_bar(&empty[s], (kb / S) & 1, a.hdr);
-        if (issued_ok) {
-          mbar_arrive_expect_tx(&full[s], stage_tx);
-          load_w(kb + S);
-          load_x(kb + S);
-        }
-      }
-    }
-    if (!__syncthreads_and(issued_ok)) {
-      ok = false;
-      break;
     }
   }
   if (tid == 0) mma_commit(done);
   __syncwarp();
   const bool fin = wait_bar(done, 0, a.hdr);
+  ok = __syncthreads_and(ok) && fin;
   tc_fence_after();
 
   // ------------------------------------------------------------------ epilogue
+  // D (TMEM lane = weight row m, column = token) goes through shared memory
+  // (the ring is idle now) as [block][token][128 rows] bf16, then out as
+  // 16-byte pieces of the contiguous output rows.
   const int row = 32 * warp + lane;    // weight row within a block = TMEM lane
   const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+  __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sm);
   for (int i = 0; i < MB; ++i) {
-    const int m = 128 * i + row;
     float sc[4] = {1.f, 1.f, 1.f, 1.f};
     if (kFp8) {
       const int nmb = (a.M + 127) / 128;
@@ -234,17 +254,23 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] += sc[b] * __uint_as_float(r[q]);
       }
-      if (!fin || !ok || m >= a.M) continue;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int t = t0 + j0 + q;
-        if (j0 + q < TN && t < a.T) {
-          if (a.mode == 0)
-            a.q_full[((size_t)t * kMaxHeads + h) * a.KQ + m] = __float2bfloat16_rn(v[q]);
-          else
-            a.out[((size_t)t * a.H + h) * a.V + m] = __float2bfloat16_rn(v[q]);
-        }
-      }
+      for (int q = 0; q < 32; ++q)
+        if (j0 + q < TN) stg[((size_t)i * TN + j0 + q) * 128 + row] = __float2bfloat16_rn(v[q]);
+    }
+  }
+  __syncthreads();
+  if (ok) {
+    // output row of (token t, block i): 128 weight rows, or fewer in the last block
+    const int chunks = MB * TN * 16;   // 16-byte pieces: 8 rows each
+    for (int c = tid; c < chunks; c += kThreads) {
+      const int piece = c & 15, tt = (c >> 4) % TN, i = (c >> 4) / TN;
+      const int t = t0 + tt, m = 128 * i + 8 * piece;
+      if (t >= a.T || m >= a.M) continue;
+      const uint4 v = *reinterpret_cast<const uint4*>(stg + ((size_t)i * TN + tt) * 128 + 8 * piece);
+      __nv_bfloat16* dst = a.mode == 0 ? a.q_full + ((size_t)t * kMaxHeads + h) * a.KQ + m
+                                       : a.out + ((size_t)t * a.H + h) * a.V + m;
+      *reinterpret_cast<uint4*>(dst) = v;
     }
   }
   if (a.mode == 0) {
@@ -352,7 +378,9 @@ cudaError_t launch(const Args& a0, WFmt wf, const void* w, const void* x, int Kx
       return cudaErrorInvalidValue;
   }
   const bool f8 = wf == WFmt::kE4M3;
-  const size_t smem = 1024 + (size_t)a.S * stage_smem + (2 * kMaxStages + 2) * 8;
+  const size_t ring_bytes = std::max((size_t)a.S * stage_smem, (size_t)a.MB * a.TN * 128 * 2);
+  const size_t smem = 1024 + ring_bytes + (2 * kMaxStages + 2) * 8;
+  if (smem > 232448) return cudaErrorInvalidValue;
   dim3 grid(1, a.H, (a.T + a.TN - 1) / a.TN);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

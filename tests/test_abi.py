@@ -102,6 +102,7 @@ def test_unsupported_shapes_are_reported(lib):
     assert _paged(lib, dims=_dims(page_size=48)) == 2              # pages must tile 64-key tiles
     assert _paged(lib, dims=_dims(qk_nope=100)) == 2               # 16-byte q / w_uk row pitch
     assert _paged(lib, dims=_dims(v_head=640)) == 2                # at most 4 w_uv row blocks
+    assert _paged(lib, dims=_dims(v_head=100)) == 2                # 16-byte output row pieces
 
 
 def test_workspace_too_small(lib):
