@@ -522,6 +522,18 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         const int s = c % S;
         if (lane == 0 && it == q_prefetch_at && next_t >= 0 && next_t < a.T)
           bulk_prefetch_l2(a.q_full + (size_t)next_t * kMaxHeads * KQ, (uint32_t)(kMaxHeads * KQ * 2));
+        if (it == q_prefetch_at && next_t < 0 && ie < tp.ntiles) {
+          // the partition's last segment ends inside its token: if this partition
+          // finishes the token last it merges the later partitions' partials
+          // (written long ago, by their first segments); bring this CTA's slices
+          // of them into L2 now (one lane per partition)
+          const int Qt = (total + a.K - 1) / a.K;
+          const int kl = (tp.tile_start + tp.ntiles - 1) / Qt;
+          const int L4 = L / 4, Hh = a.d.num_heads;
+          for (int kk = k + 1 + lane; kk <= kl; kk += 32)
+            bulk_prefetch_l2(reinterpret_cast<const float4*>(a.part_o) + ((size_t)(kk * 2) * L4 + lat_x0 / 4) * Hh,
+                             (uint32_t)(LC * Hh * 4));
+        }
         // global reads, issued before the wait for the stage so their latency overlaps it
         bool v[2];
         int rid[2], pg[2];
@@ -661,35 +673,28 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         tc_fence_after();
         const uint64_t dk = dk0 + (uint64_t)((s * C::kStageBytes) >> 4);
         const uint32_t sd = tmem + C::kSCol + 64 * b;
-        // latent [0, QT): A = query in TMEM; the MMA queue is shallow, so the
-        // issue runs back to back
-#pragma unroll
-        for (int j = 0; j < C::QT / 64; ++j) {
-          if (lane == 0) {
+        // latent [0, QT): A = query in TMEM; then latent [QT, L) and the rope
+        // (64 columns; past qk_rope both sides read the TMA zero fill) with A =
+        // query boxes in shared memory.  The MMA queue is shallow, so the issue
+        // runs back to back; the box loops stay rolled to keep the code small.
+        if (lane == 0) {
+#pragma unroll 1
+          for (int j = 0; j < C::QT / 64; ++j) {
+            const uint64_t dkj = dk + (uint64_t)((j * C::kBox) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(sd, tmem + C::kQCol + 8 * (4 * j + kk), dk + (uint64_t)((j * C::kBox + kk * 32) >> 4), idesc_qk,
+              mma_ts(sd, tmem + C::kQCol + 8 * (4 * j + kk), dkj + (uint64_t)((kk * 32) >> 4), idesc_qk,
                      (j > 0 || kk > 0) ? 1u : 0u);
           }
-          __syncwarp();
-        }
-        // latent [QT, L): A = query boxes in shared memory
-#pragma unroll
-        for (int i = 0; i < C::NQS; ++i) {
-          if (lane == 0) {
+#pragma unroll 1
+          for (int i = 0; i <= C::NQS; ++i) {
+            // box i of the query buffer pairs with cache box QT / 64 + i (the rope box after the latent ones)
+            const uint64_t dqi = dq0 + (uint64_t)((i * C::kQBox) >> 4);
+            const uint64_t dki = dk + (uint64_t)(((C::QT / 64 + i) * C::kBox) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(sd, dq0 + (uint64_t)((i * C::kQBox + kk * 32) >> 4),
-                     dk + (uint64_t)(((C::QT / 64 + i) * C::kBox + kk * 32) >> 4), idesc_qk, 1u);
+              mma_ss(sd, dqi + (uint64_t)((kk * 32) >> 4), dki + (uint64_t)((kk * 32) >> 4), idesc_qk, 1u);
           }
-          __syncwarp();
-        }
-        // rope (64 columns; past qk_rope both sides read the TMA zero fill)
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(sd, dq0 + (uint64_t)((C::NQS * C::kQBox + kk * 32) >> 4),
-                   dk + (uint64_t)((C::NLB * C::kBox + kk * 32) >> 4), idesc_qk, 1u);
           mma_commit(&cs->s_full[b]);
           // the segment's last QK: its query buffers may be refilled once it completes
           if (it + 1 == ie) mma_commit(&cs->q_empty);

@@ -67,6 +67,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, PlanHea
   atomicOr(&hdr->status, kDeviceTimeout);
   return false;
 }
+// The k loop's issuing thread spins instead (a suspended waiter can wake well
+// after the phase completes).
+__device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, PlanHeader* hdr) {
+  if (mbar_spin(bar, parity, kWaitLimitNs)) return true;
+  atomicOr(&hdr->status, kDeviceTimeout);
+  return false;
+}
 
 // e4m3 byte pair -> bf16x2 through the exact fp8 -> half conversion.
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
@@ -164,26 +171,58 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     mma_commit(&empty[s]);
     if (kb + S < nkb) {
       // the stage is refilled once the MMAs above have read it
-      if (!wait_bar(&empty[s], (kb / S) & 1, a.hdr)) return false;
+      if (!spin_bar(&empty[s], (kb / S) & 1, a.hdr)) return false;
       mbar_arrive_expect_tx(&full[s], stage_tx);
       load_w(kb + S);
       load_x(kb + S);
     }
     return true;
   };
+  // absorb: the rope columns of q go to q_full unchanged (independent of the
+  // GEMM, so done while the MMAs run), 16 bytes at a time with every load of a
+  // thread issued before its stores (q and q_full may not alias, but the
+  // compiler cannot know that); absent heads are zero rows
+  auto copy_rope = [&](int first, int stride) {
+    const int cpr = a.R / 8;   // 16-byte chunks per (token, head) row
+    constexpr int kBatch = 8;
+    for (int i0 = first; i0 < TN * cpr; i0 += stride * kBatch) {
+      uint4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * stride, t = t0 + i / cpr;
+        if (i < TN * cpr && t < a.T)
+          v[j] = __ldg(reinterpret_cast<const uint4*>(a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N) + i % cpr);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * stride, t = t0 + i / cpr;
+        if (i < TN * cpr && t < a.T)
+          reinterpret_cast<uint4*>(a.q_full + ((size_t)t * kMaxHeads + h) * a.KQ + a.L)[i % cpr] = v[j];
+      }
+    }
+    if (h == 0 && a.H < kMaxHeads) {
+      const int per = (kMaxHeads - a.H) * a.KQ;
+      for (int i = first; i < TN * per; i += stride) {
+        const int t = t0 + i / per;
+        if (t < a.T) a.q_full[((size_t)t * kMaxHeads + a.H) * a.KQ + i % per] = __float2bfloat16_rn(0.f);
+      }
+    }
+  };
   bool ok = true;
   if (!kFp8) {
     // one thread runs the whole k loop; the others only wait for the result
+    if (a.mode == 0 && warp > 0) copy_rope(tid - 32, kThreads - 32);
     if (tid == 0) {
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int s = kb % S;
-        ok = wait_bar(&full[s], (kb / S) & 1, a.hdr);
+        ok = spin_bar(&full[s], (kb / S) & 1, a.hdr);
         if (!ok) break;
         tc_fence_after();
         ok = issue(kb, s);
       }
     }
   } else {
+    if (a.mode == 0) copy_rope(tid, kThreads);
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % S;
       // every thread waits; the CTA proceeds only if all saw the stage arrive
@@ -261,49 +300,22 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   }
   __syncthreads();
   if (ok) {
-    // output row of (token t, block i): 128 weight rows, or fewer in the last block
-    const int chunks = MB * TN * 16;   // 16-byte pieces: 8 rows each
-    for (int c = tid; c < chunks; c += kThreads) {
-      const int piece = c & 15, tt = (c >> 4) % TN, i = (c >> 4) / TN;
-      const int t = t0 + tt, m = 128 * i + 8 * piece;
-      if (t >= a.T || m >= a.M) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(stg + ((size_t)i * TN + tt) * 128 + 8 * piece);
-      __nv_bfloat16* dst = a.mode == 0 ? a.q_full + ((size_t)t * kMaxHeads + h) * a.KQ + m
-                                       : a.out + ((size_t)t * a.H + h) * a.V + m;
-      *reinterpret_cast<uint4*>(dst) = v;
+    // output row of (token t, block i): 128 weight rows (fewer in the last
+    // block) as 16 pieces of 16 bytes; 8 rows of 16 threads per pass
+    const int piece = tid & 15;
+    const int ntok = min(TN, a.T - t0);
+    for (int i = 0; i < MB; ++i) {
+      const int m = 128 * i + 8 * piece;
+      if (m >= a.M) continue;
+      const __nv_bfloat16* src = stg + (size_t)i * TN * 128 + 8 * piece;
+      __nv_bfloat16* dst = a.mode == 0 ? a.q_full + ((size_t)t0 * kMaxHeads + h) * a.KQ + m
+                                       : a.out + ((size_t)t0 * a.H + h) * a.V + m;
+      const size_t dst_pitch = a.mode == 0 ? (size_t)kMaxHeads * a.KQ : (size_t)a.H * a.V;
+      for (int tt = tid >> 4; tt < ntok; tt += kThreads / 16)
+        *reinterpret_cast<uint4*>(dst + tt * dst_pitch) = *reinterpret_cast<const uint4*>(src + tt * 128);
     }
   }
-  if (a.mode == 0) {
-    // rope columns are copied unchanged, 16 bytes at a time; every load of the
-    // thread is issued before its stores (q and q_full may not alias, but the
-    // compiler cannot know that)
-    {
-      const int cpr = a.R / 8;   // 16-byte chunks per (token, head) row
-      constexpr int kBatch = 8;
-      for (int i0 = tid; i0 < TN * cpr; i0 += kThreads * kBatch) {
-        uint4 v[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-          const int i = i0 + j * kThreads, t = t0 + i / cpr;
-          if (i < TN * cpr && t < a.T)
-            v[j] = __ldg(reinterpret_cast<const uint4*>(a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N) + i % cpr);
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-          const int i = i0 + j * kThreads, t = t0 + i / cpr;
-          if (i < TN * cpr && t < a.T)
-            reinterpret_cast<uint4*>(a.q_full + ((size_t)t * kMaxHeads + h) * a.KQ + a.L)[i % cpr] = v[j];
-        }
-      }
-    }
-    if (h == 0 && a.H < kMaxHeads) {
-      const int per = (kMaxHeads - a.H) * a.KQ;
-      for (int i = tid; i < TN * per; i += kThreads) {
-        const int t = t0 + i / per;
-        if (t < a.T) a.q_full[((size_t)t * kMaxHeads + a.H) * a.KQ + i % per] = __float2bfloat16_rn(0.f);
-      }
-    }
-  } else if (a.lse_out) {
+  if (a.mode == 1 && a.lse_out) {
     for (int j = tid; j < TN; j += kThreads)
       if (t0 + j < a.T) a.lse_out[(size_t)(t0 + j) * a.H + h] = a.lse_ws[(size_t)(t0 + j) * a.H + h];
   }
