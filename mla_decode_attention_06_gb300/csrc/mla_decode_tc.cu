@@ -73,6 +73,7 @@ struct Smem {   // control block after the stage ring
   uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
   uint64_t fix_bar, fix_done;    // softmax: partial written / merge decision published
   uint64_t mrg_full, mrg_done;   // merge: a partial landed in the idle stage ring / was read
+  uint64_t mrg_sync;             // merge: the 128 softmax threads, bounded
   uint64_t bye;                  // the peer CTA is done touching this CTA's shared memory
   int32_t rowid[kMaxStages][64]; // physical row of each tile row (kLoadFp8, kLoadSparse)
   uint32_t tmem_base;
@@ -285,23 +286,46 @@ __device__ __forceinline__ bool waborted(const Smem* cs) { return __any_sync(0xf
 // query columns, idle after the last QK).  Warp-uniform; false on a time-out.
 __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t, const TokenPlan& tp, int k, int kf,
                                            int kl, int Qt, uint32_t rank, int row, int lat_x0, int LC, uint32_t trow,
-                                           uint32_t tacc, float lse_own, float inv, uint8_t* ring, int& nmrg) {
+                                           uint32_t tacc, float lse_own, float inv, uint8_t* ring, int& nmrg,
+                                           int& nsync) {
   const int H = a.d.num_heads, L = a.d.kv_lora_rank;
   PlanHeader* hdr = a.hdr_mut;
   const bool live = row < H;
   auto slot_of = [&](int kk) { return (kk == kf && tp.tile_start != kk * Qt) ? 1 : 0; };
-  auto lse_of = [&](int kk) {
-    return kk == k ? lse_own : __ldcg(a.part_lse + ((size_t)(kk * 2 + slot_of(kk)) * 2 + rank) * H + row);
+  auto lse_ptr = [&](int kk) { return a.part_lse + ((size_t)(kk * 2 + slot_of(kk)) * 2 + rank) * H + row; };
+  // max, then sum over p in order of e^(lse_p - max), as the general form does;
+  // up to eight partitions' log-sum-exps are loaded once, eight at a time
+  const int np = kl - kf + 1;
+  float lv0[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int kk = kf + j;
+    lv0[j] = kk > kl ? -CUDART_INF_F : (kk == k ? lse_own : __ldcg(lse_ptr(kk)));
+  }
+  auto lse_at = [&](int kk) {
+    if (kk - kf < 8) {
+      float v = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v = (kk - kf == j) ? lv0[j] : v;
+      return v;
+    }
+    return kk == k ? lse_own : __ldcg(lse_ptr(kk));
   };
   float mx = -CUDART_INF_F;
-  for (int kk = kf; kk <= kl; ++kk) mx = fmaxf(mx, lse_of(kk));
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mx = fmaxf(mx, lv0[j]);
+  for (int kk = kf + 8; kk <= kl; ++kk) mx = fmaxf(mx, lse_at(kk));
   float sum = 0.f;
-  if (mx != -CUDART_INF_F)
-    for (int kk = kf; kk <= kl; ++kk) sum += __expf(lse_of(kk) - mx);
+  if (mx != -CUDART_INF_F) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < np) sum += __expf(lv0[j] - mx);
+    for (int kk = kf + 8; kk <= kl; ++kk) sum += __expf(lse_at(kk) - mx);
+  }
   const float inv_sum = sum > 0.f ? 1.f / sum : 0.f;
   const float4* sp = reinterpret_cast<const float4*>(ring);
   for (int kk = kf; kk <= kl; ++kk) {
-    const float w = mx != -CUDART_INF_F ? __expf(lse_of(kk) - mx) * inv_sum : 0.f;
+    const float w = mx != -CUDART_INF_F ? __expf(lse_at(kk) - mx) * inv_sum : 0.f;
     const bool own = kk == k, first = kk == kf;
     if (!own) {
       bool ok = true;
@@ -318,27 +342,37 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
       if (!__all_sync(0xffffffffu, ok)) return false;
       if (!wwait(&cs->mrg_full, nmrg & 1, cs, hdr)) return false;
     }
+    // 32 columns per step, every load of the step in flight before one wait
+    if (own) {
 #pragma unroll 1
-    for (int col = 0; col < LC; col += 16) {
-      uint32_t u[16], acc[16];
-      if (own) tmem_ld16(trow + col, u);
-      if (!first) tmem_ld16(tacc + col, acc);
-      tmem_ld_wait();
+      for (int col = 0; col < LC; col += 32) {
+        uint32_t u[32], acc[32];
+        tmem_ld32(trow + col, u);
+        if (!first) tmem_ld32(tacc + col, acc);
+        tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float v[4];
-        if (own) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(u[4 * i + j]) * inv;
-        } else {
-          const float4 x = live ? sp[(col / 4 + i) * H + row] : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          acc[4 * i + j] = __float_as_uint(fmaf(w, v[j], first ? 0.f : __uint_as_float(acc[4 * i + j])));
+        for (int j = 0; j < 32; ++j)
+          acc[j] = __float_as_uint(fmaf(w, __uint_as_float(u[j]) * inv, first ? 0.f : __uint_as_float(acc[j])));
+        tmem_st32(tacc + col, acc);
       }
-      tmem_st16(tacc + col, acc);
+    } else {
+#pragma unroll 1
+      for (int col = 0; col < LC; col += 32) {
+        uint32_t acc[32];
+        if (!first) tmem_ld32(tacc + col, acc);
+        float4 x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = live ? sp[(col / 4 + i) * H + row] : make_float4(0.f, 0.f, 0.f, 0.f);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float v[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            acc[4 * i + j] = __float_as_uint(fmaf(w, v[j], first ? 0.f : __uint_as_float(acc[4 * i + j])));
+        }
+        tmem_st32(tacc + col, acc);
+      }
     }
     tmem_st_wait();
     if (!own) {
@@ -346,19 +380,49 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
       ++nmrg;
     }
   }
-  // the merged row: bf16 latent output and its log-sum-exp
+  // the merged row as bf16, staged row-major in the idle ring (after the last
+  // partial there has been read by every thread), then written out so that a
+  // warp's store covers 512 contiguous bytes of one output row
+  bool synced = !(nmrg > 0 && row == 0 && !wait_or_abort(&cs->mrg_done, (nmrg - 1) & 1, cs, hdr));
+  auto sync128 = [&]() {   // short waits: spin rather than suspend
+    mbar_arrive(&cs->mrg_sync);
+    bool ok = mbar_spin(&cs->mrg_sync, nsync & 1, kWaitLimitNs);
+    if (!ok) {
+      record_timeout(&cs->mrg_sync, hdr);
+      atomicOr(&hdr->status, kDeviceTimeout);
+      *reinterpret_cast<volatile int*>(&cs->abort) = 1;
+    }
+    ++nsync;
+    return __all_sync(0xffffffffu, ok);
+  };
+  if (!__all_sync(0xffffffffu, synced) || !sync128()) return false;
+  __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(ring);
 #pragma unroll 1
-  for (int col = 0; col < LC; col += 16) {
-    uint32_t r[16];
-    tmem_ld16(tacc + col, r);
+  for (int col = 0; col < LC; col += 32) {
+    uint32_t r[32];
+    tmem_ld32(tacc + col, r);
     tmem_ld_wait();
-    if (!live) continue;
-    uint32_t o[8];
+    uint32_t o[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-    uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + row) * L + lat_x0 + col);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    for (int i = 0; i < 16; ++i) o[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+    // row-major [128][LC] with the 16-byte chunk index rotated by the row, so
+    // a warp's 32 rows write different banks
+    uint4* rowp = reinterpret_cast<uint4*>(stg + (size_t)row * LC);
+    const int nch = LC / 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      rowp[(col / 8 + i + row) % nch] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  }
+  if (!sync128()) return false;
+  {
+    const int nch = LC / 8;                 // 16-byte chunks per row half
+    const int tid4 = row;                   // 0..127 over the four softmax warps
+    for (int idx = tid4; idx < 128 * nch; idx += 128) {
+      const int rr = idx / nch, ch = idx % nch;
+      if (rr >= H) continue;
+      const uint4 v = reinterpret_cast<const uint4*>(stg + (size_t)rr * LC)[(ch + rr) % nch];
+      reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + rr) * L + lat_x0)[ch] = v;
+    }
   }
   if (live && rank == 0) a.lse_ws[(size_t)t * H + row] = mx != -CUDART_INF_F ? mx + __logf(sum) : -CUDART_INF_F;
   return true;
@@ -415,6 +479,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     mbar_init(&cs->fix_done, 1);
     mbar_init(&cs->mrg_full, 1);
     mbar_init(&cs->mrg_done, 128);
+    mbar_init(&cs->mrg_sync, 128);
     mbar_init(&cs->bye, 1);
     cs->abort = 0;
     fence_mbar_init();
@@ -530,9 +595,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           const int Qt = (total + a.K - 1) / a.K;
           const int kl = (tp.tile_start + tp.ntiles - 1) / Qt;
           const int L4 = L / 4, Hh = a.d.num_heads;
-          for (int kk = k + 1 + lane; kk <= kl; kk += 32)
+          for (int kk = k + 1 + lane; kk <= kl; kk += 32) {
             bulk_prefetch_l2(reinterpret_cast<const float4*>(a.part_o) + ((size_t)(kk * 2) * L4 + lat_x0 / 4) * Hh,
                              (uint32_t)(LC * Hh * 4));
+            bulk_prefetch_l2(a.part_lse + (size_t)(kk * 2) * 2 * Hh, (uint32_t)(2 * Hh * 4));
+          }
         }
         // global reads, issued before the wait for the stage so their latency overlaps it
         bool v[2];
@@ -820,6 +887,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     int c = 0;
     int nfix = 0;   // split-token merges attempted (phase of fix_bar / fix_done)
     int nmrg = 0;   // partials brought in by bulk copy (phase of mrg_full / mrg_done)
+    int nsync = 0;  // merge-wide syncs (phase of mrg_sync)
     bool q_ready = false;   // the coming segment's query is already in TMEM
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
                                      int next_t) {
@@ -1005,7 +1073,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             // This was the partition's last segment: O in TMEM still holds this
             // CTA's own partial and the stage ring is idle.
             if (!merge_in_tmem(a, cs, t, tp, k, kf, kl, Qt, rank, row, lat_x0, LC, trow, trow + C::kSCol, lse, inv,
-                               sStage, nmrg))
+                               sStage, nmrg, nsync))
               return;
           } else if (live) {
             merge_split_token(a, t, tp, kf, kl, Qt, rank, row, lat_x0, LC);
