@@ -25,7 +25,7 @@
 // 128B-swizzled shared memory.  TMEM: O (256) | S, two 64-column buffers |
 // Q latent (128).  Narrow latents (64) run the same code on one CTA.
 //
-// Warp roles (224 threads; 288 with the converter warps of an e4m3 cache):
+// Warp roles (224 threads; 352 with the converter warps of an e4m3 cache):
 //   warp 0      TMA producer: the query's shared-memory part once per segment,
 //               cache tiles through the page table into a kStages-deep ring,
 //               and an L2 prefetch of the tile two ahead.
@@ -37,7 +37,7 @@
 //               domain, writes P (bf16 pairs) back into TMEM where the P . C
 //               MMA takes it as its A operand, rescales O only when the running
 //               max grows by more than 2^8, and writes the segment's output.
-//   warps 6-7   (e4m3 cache) widen the tile's codes x row scale into bf16.
+//   warps 6-9   (e4m3 cache) widen the tile's codes x row scale into bf16.
 //   last warp   P . C issuer (one thread), so a ready P never waits behind a QK.
 // Every wait is bounded in time; a timeout sets a status bit and the kernel
 // unwinds without hanging.
@@ -100,8 +100,8 @@ struct Cfg {
   static constexpr int RW = L < 256 ? L : 256;      // e4m3 bytes per raw box row
   static constexpr int NRH = L / RW;                // raw boxes per cached row
   static constexpr int kRawOff = NLB >= 8 ? 4 * kBox : 0;   // codes land where the last latent boxes go
-  static constexpr int kConvThreads = 64;                      // warps 6-7 (kLoadFp8)
-  static constexpr int kPvWarp = kMode == kLoadFp8 ? 8 : 6;    // the P . C issuer
+  static constexpr int kConvThreads = 64 * NRH;                // warps 6.. (kLoadFp8): one per row and raw box
+  static constexpr int kPvWarp = kMode == kLoadFp8 ? 6 + kConvThreads / 32 : 6;   // the P . C issuer
   static constexpr int kThreads = 32 * (kPvWarp + 1);
   static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + (int)sizeof(Smem);
   static_assert(LC % 64 == 0 && (CL == 1 || CL == 2), "latent slice");
@@ -185,6 +185,16 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
       "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
+// The same four rows delivered to every CTA of the cluster in `cta_mask`.
+__device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y0, int y1,
+                                               int y2, int y3, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "h"(cta_mask)
       : "memory");
 }
 
@@ -616,20 +626,35 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         uint8_t* st = sStage + s * C::kStageBytes;
         uint8_t* st_rope = st + C::NLB * C::kBox;
         if (MODE == kLoadSparse) {
-          // every row is fetched by each CTA (row 0 stands in for a dead slot; its P . C part is zeroed)
+          // every row is fetched (row 0 stands in for a dead slot; its P . C part is zeroed);
+          // each CTA gathers half of the boxes and multicasts them to both
           if (lane == 0) {
             cs->row_mask[s] = mask;
             mbar_arrive_expect_tx(&cs->kv_full[s], 64 * (C::NLB + 1) * 128);
           }
           __syncwarp();
           if (lane < 16) {
+            // this CTA's share of the boxes (both CTAs see the same rows), multicast
             const int r0 = 4 * lane;
             const int y0 = cs->rowid[s][r0], y1 = cs->rowid[s][r0 + 1];
             const int y2 = cs->rowid[s][r0 + 2], y3 = cs->rowid[s][r0 + 3];
+            constexpr int kOwnBoxes = C::NLB / CL;
 #pragma unroll
-            for (int i = 0; i < C::NLB; ++i)
-              tma_gather4(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y0, y1, y2, y3);
-            tma_gather4(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y0, y1, y2, y3);
+            for (int j = 0; j < kOwnBoxes; ++j) {
+              const int i = (int)rank * kOwnBoxes + j;
+              if (CL == 2)
+                tma_gather4_mc(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y0, y1, y2, y3,
+                               (uint16_t)0x3);
+              else
+                tma_gather4(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y0, y1, y2, y3);
+            }
+            if (rank == 0) {
+              if (CL == 2)
+                tma_gather4_mc(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y0, y1, y2, y3,
+                               (uint16_t)0x3);
+              else
+                tma_gather4(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y0, y1, y2, y3);
+            }
           }
         } else {
           // pages of this tile that hold at least one live row; both CTAs count the
@@ -803,12 +828,12 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     });
   } else if (MODE == kLoadFp8 && warp >= 6) {
     // ------------------------------------------------------------- e4m3 converters
-    // thread ci widens tile row ci: L e4m3 codes x row scale -> bf16 in the
-    // 128B-swizzled latent boxes; dead rows become zeros (latent and rope).
-    // The codes sit where the last latent boxes go (L = 512: boxes 4-7; L = 64:
-    // box 0), so every thread reads the codes of the last raw box before anyone
-    // writes those boxes.
-    const int ci = tid - 192;
+    // thread ci widens raw box h = ci / 64 of tile row ci % 64: RW e4m3 codes x
+    // row scale -> bf16 in the 128B-swizzled latent boxes; dead rows become zeros
+    // (latent and rope).  The codes sit where the last raw box's latent boxes go
+    // (L = 512: boxes 4-7; L = 64: box 0), so the threads writing those boxes
+    // wait until every thread has read its codes.
+    const int ci = tid - 192, crow = ci & 63, h = ci >> 6;
     int c = 0;
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++c) {
@@ -816,36 +841,31 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         const int s = c % S;
         if (!wwait(&cs->kv_full[s], (c / S) & 1, cs, hdr)) return;
         uint8_t* st = sStage + s * C::kStageBytes;
-        const bool live = (cs->row_mask[s] >> ci) & 1ull;
-        const float sc = live ? a.kv_scales[cs->rowid[s][ci]] : 0.f;
-#pragma unroll 1
-        for (int h = 0; h < C::NRH; ++h) {
-          uint4 raw[C::RW / 16];
-          const uint8_t* src = st + C::kRawOff + h * 64 * C::RW + ci * C::RW;
+        const bool live = (cs->row_mask[s] >> crow) & 1ull;
+        const float sc = live ? a.kv_scales[cs->rowid[s][crow]] : 0.f;
+        uint4 raw[C::RW / 16];
+        const uint8_t* src = st + C::kRawOff + h * 64 * C::RW + crow * C::RW;
 #pragma unroll
-          for (int q = 0; q < C::RW / 16; ++q) raw[q] = *reinterpret_cast<const uint4*>(src + q * 16);
-          if (h == C::NRH - 1) {
-            mbar_arrive(&cs->conv_sync);
-            if (!wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
+        for (int q = 0; q < C::RW / 16; ++q) raw[q] = *reinterpret_cast<const uint4*>(src + q * 16);
+        mbar_arrive(&cs->conv_sync);
+        if (h == C::NRH - 1 && !wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
+#pragma unroll
+        for (int q = 0; q < C::RW / 16; ++q) {
+          const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
+            o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
           }
-#pragma unroll
-          for (int q = 0; q < C::RW / 16; ++q) {
-            const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
-            uint32_t o[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
-              o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
-            }
-            const int col = h * C::RW + 16 * q;      // first latent column of this chunk pair
-            uint8_t* box = st + (col >> 6) * C::kBox + ci * 128;
-            const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
-            *reinterpret_cast<uint4*>(box + (((ch) ^ (ci & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (ci & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-          }
+          const int col = h * C::RW + 16 * q;      // first latent column of this chunk pair
+          uint8_t* box = st + (col >> 6) * C::kBox + crow * 128;
+          const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
+          *reinterpret_cast<uint4*>(box + (((ch) ^ (crow & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (crow & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        if (!live) {
-          uint4* rr = reinterpret_cast<uint4*>(st + C::NLB * C::kBox + ci * 128);
+        if (!live && h == 0) {
+          uint4* rr = reinterpret_cast<uint4*>(st + C::NLB * C::kBox + crow * 128);
 #pragma unroll
           for (int i = 0; i < 8; ++i) rr[i] = make_uint4(0, 0, 0, 0);
         }
