@@ -43,6 +43,8 @@
 // unwinds without hanging.
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "mla_kernels.cuh"
 #include "sm100_ptx.cuh"
 
@@ -1158,6 +1160,52 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The tensor maps of a launch depend only on these; consecutive calls on the
+// same buffers (the serving loop) reuse the last encoding.
+struct MapKey {
+  int device;
+  const void* kv_pool;
+  const void* q_full;
+  int L, R, ps, num_pages, T;
+  bool operator==(const MapKey& o) const {
+    return device == o.device && kv_pool == o.kv_pool && q_full == o.q_full && L == o.L && R == o.R && ps == o.ps &&
+           num_pages == o.num_pages && T == o.T;
+  }
+};
+
+}  // namespace tc
+
+cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  // (kernel, device) pairs whose limit is already raised; a handful of kernels
+  struct Entry {
+    const void* func;
+    int device, bytes;
+  };
+  static std::mutex mu;
+  static Entry done[64];
+  static int n = 0;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < n; ++i) {
+    if (done[i].func == func && done[i].device == device) {
+      if (done[i].bytes >= bytes) return cudaSuccess;
+      slot = i;
+    }
+  }
+  // the limit counts dynamic bytes only (static shared memory comes on top), so
+  // it is raised to exactly what this launch needs, and again if a later one needs more
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  if (slot >= 0) done[slot].bytes = bytes;
+  else if (n < 64) done[n++] = Entry{func, device, bytes};
+  return cudaSuccess;
+}
+
+namespace tc {
+
 template <int LC, int CL, int MODE>
 cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
   using C = Cfg<LC, CL, MODE>;
@@ -1165,23 +1213,41 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
   const int L = a.d.kv_lora_rank, R = a.d.qk_rope, KQ = L + R, ps = a.d.page_size;
   const uint32_t rows = MODE == kLoadSparse ? 1u : (uint32_t)(ps < kTileKeys ? ps : kTileKeys);
   const uint64_t pool_rows = (uint64_t)a.d.num_pages * ps;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return cudaErrorInvalidDevice;
+  const MapKey key{device, a.kv_pool, a.q_full, L, R, ps, a.d.num_pages, a.T};
+  static std::mutex cache_mu;
+  static bool cache_valid = false;
+  static MapKey cache_key;
+  static Maps cache_maps;
   Maps maps;
-  bool ok;
-  if (MODE == kLoadFp8) {
-    const uint64_t rb = (uint64_t)L + 2 * R;   // bytes per cached row
-    ok = encode_2d(&maps.kv_lat, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv_pool, rb, pool_rows, rb, C::RW, rows,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         encode_2d(&maps.kv_rope, kBF16, a.kv_pool, rb / 2, pool_rows, rb, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
-  } else {
-    ok = encode_2d(&maps.kv_lat, kBF16, a.kv_pool, KQ, pool_rows, (uint64_t)KQ * 2, 64, rows,
-                   CU_TENSOR_MAP_SWIZZLE_128B);
-    maps.kv_rope = maps.kv_lat;   // the rope box is one more 64-column box of the same rows
+  bool hit;
+  {
+    std::lock_guard<std::mutex> lock(cache_mu);
+    hit = cache_valid && cache_key == key;
+    if (hit) maps = cache_maps;
   }
-  ok = ok && encode_2d(&maps.q, kBF16, a.q_full, KQ, (uint64_t)a.T * kMaxHeads, (uint64_t)KQ * 2, 64, 128,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<LC, CL, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmem);
+  if (!hit) {
+    bool ok;
+    if (MODE == kLoadFp8) {
+      const uint64_t rb = (uint64_t)L + 2 * R;   // bytes per cached row
+      ok = encode_2d(&maps.kv_lat, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.kv_pool, rb, pool_rows, rb, C::RW, rows,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode_2d(&maps.kv_rope, kBF16, a.kv_pool, rb / 2, pool_rows, rb, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      ok = encode_2d(&maps.kv_lat, kBF16, a.kv_pool, KQ, pool_rows, (uint64_t)KQ * 2, 64, rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+      maps.kv_rope = maps.kv_lat;   // the rope box is one more 64-column box of the same rows
+    }
+    ok = ok && encode_2d(&maps.q, kBF16, a.q_full, KQ, (uint64_t)a.T * kMaxHeads, (uint64_t)KQ * 2, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return cudaErrorInvalidValue;
+    std::lock_guard<std::mutex> lock(cache_mu);
+    cache_key = key;
+    cache_maps = maps;
+    cache_valid = true;
+  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<LC, CL, MODE>), C::kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.K * CL);

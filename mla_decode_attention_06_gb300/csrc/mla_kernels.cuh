@@ -31,6 +31,10 @@ struct DecodeArgs {
 
 
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device (the
+// driver call costs microseconds per launch otherwise).  Thread-safe.
+cudaError_t ensure_smem_limit(const void* func, int bytes);
+
 // Tensor-core decode (tcgen05): dense bf16 paged cache, shapes listed in decode_tc_supported.
 bool decode_tc_supported(const mla_dims_t& d);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
