@@ -74,8 +74,7 @@ struct Smem {   // control block after the stage ring
   uint64_t o_free;
   uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
   uint64_t fix_bar, fix_done;    // softmax: partial written / merge decision published
-  uint64_t mrg_full, mrg_done;   // merge: a partial landed in the idle stage ring / was read
-  uint64_t mrg_sync;             // merge: the 128 softmax threads, bounded
+  uint64_t mrg_full[2], mrg_done[2];   // merge: a half partial landed in its buffer / was read
   uint64_t bye;                  // the peer CTA is done touching this CTA's shared memory
   int32_t rowid[kMaxStages][64]; // physical row of each tile row (kLoadFp8, kLoadSparse)
   uint32_t tmem_base;
@@ -105,9 +104,13 @@ struct Cfg {
   static constexpr int kConvThreads = 64 * NRH;                // warps 6.. (kLoadFp8): one per row and raw box
   static constexpr int kPvWarp = kMode == kLoadFp8 ? 6 + kConvThreads / 32 : 6;   // the P . C issuer
   static constexpr int kThreads = 32 * (kPvWarp + 1);
-  static constexpr int kSmem = 1024 + kQBytes + kStages * kStageBytes + (int)sizeof(Smem);
+  static constexpr int kRegionBytes = kQBytes + kStages * kStageBytes;   // query buffer + stage ring
+  static constexpr int kMrgHalf = (LC / 2) * kMaxHeads * 4;               // merge: one half partial slice
+  static constexpr int kStgBytes = kMaxHeads * (LC * 2 + 16);             // merge: staged output rows
+  static constexpr int kSmem = 1024 + kRegionBytes + (int)sizeof(Smem);
   static_assert(LC % 64 == 0 && (CL == 1 || CL == 2), "latent slice");
   static_assert(kQCol + QT / 2 <= 512, "TMEM columns");
+  static_assert(kStgBytes + 2 * kMrgHalf <= kRegionBytes, "merge buffers in the idle region");
   static_assert(NRH % CL == 0, "raw boxes split over the cluster");
   static_assert(QT / 64 <= NQS + 1, "the query staging fits the query buffer");
   static_assert(kSmem <= 232448, "shared memory");
@@ -290,24 +293,52 @@ __device__ __forceinline__ bool waborted(const Smem* cs) { return __any_sync(0xf
 
 // The merge of a split token by a CTA whose last segment it was: O in TMEM
 // still holds this CTA's own partial (unnormalised; 1 / row sum = inv) and the
-// stage ring is idle.  Each other partition's slice of its partial (one
-// contiguous block of the interleaved layout) comes in with one bulk copy into
-// the ring.  acc = sum over partitions, in order, of fmaf(w_p, o_p, acc) from
-// zero: the operations and order of merge_split_token, so the bits do not
-// depend on which partition merges.  acc lives in TMEM at `tacc` (the S and
-// query columns, idle after the last QK).  Warp-uniform; false on a time-out.
+// query buffer and stage ring are idle.  Each other partition's slice of its
+// partial (one contiguous block of the interleaved layout) comes in as two
+// halves of LC / 2 columns by bulk copy, double-buffered at the end of the idle
+// region, the first two issued before the weights are known.  acc = sum over
+// partitions, in order, of fmaf(w_p, o_p, acc) from zero: the operations and
+// order of merge_split_token, so the bits do not depend on which partition
+// merges.  acc lives in TMEM at `tacc` (the S and query columns, idle after
+// the last QK).  Each thread stages its own bf16 output row at the start of the
+// region (rows padded by 16 bytes) and writes it with one bulk copy.
+// Warp-uniform; false on a time-out.
+template <int LC>
 __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t, const TokenPlan& tp, int k, int kf,
-                                           int kl, int Qt, uint32_t rank, int row, int lat_x0, int LC, uint32_t trow,
-                                           uint32_t tacc, float lse_own, float inv, uint8_t* ring, int& nmrg,
-                                           int& nsync) {
+                                           int kl, int Qt, uint32_t rank, int row, int lat_x0, uint32_t trow,
+                                           uint32_t tacc, float lse_own, float inv, uint8_t* stg, uint8_t* hb,
+                                           int& nmrg) {
+  constexpr int LH = LC / 2;                            // columns per half slice
+  constexpr uint32_t kHalf = (uint32_t)LH * kMaxHeads * 4;
+  constexpr int kStgStride = LC * 2 + 16;               // bytes per staged row
   const int H = a.d.num_heads, L = a.d.kv_lora_rank;
   PlanHeader* hdr = a.hdr_mut;
   const bool live = row < H;
   auto slot_of = [&](int kk) { return (kk == kf && tp.tile_start != kk * Qt) ? 1 : 0; };
   auto lse_ptr = [&](int kk) { return a.part_lse + ((size_t)(kk * 2 + slot_of(kk)) * 2 + rank) * H + row; };
+  const int np = kl - kf + 1;
+  const int nj = 2 * (np - 1);                          // half slices to bring in
+  const uint32_t half_bytes = (uint32_t)(LH * H * 4);
+  auto issue = [&](int j) {                             // thread row 0: bring in half slice j
+    const int g = nmrg + j, b = g & 1;
+    if (g >= 2 && !wait_or_abort(&cs->mrg_done[b], ((g - 2) >> 1) & 1, cs, hdr)) return false;
+    int p = kf + (j >> 1);
+    if (p >= k) ++p;
+    mbar_arrive_expect_tx(&cs->mrg_full[b], half_bytes);
+    bulk_copy_g2s(hb + b * kHalf,
+                  reinterpret_cast<const float4*>(a.part_o) + part_index(p, slot_of(p), lat_x0 / 4 + (j & 1) * (LH / 4), 0, L, H),
+                  half_bytes, &cs->mrg_full[b]);
+    return true;
+  };
+  bool ok = true;
+  if (row == 0) {
+    fence_proxy_async_global();
+    if (nj > 0) ok = issue(0);
+    if (ok && nj > 1) ok = issue(1);
+  }
+  if (!__all_sync(0xffffffffu, ok)) return false;
   // max, then sum over p in order of e^(lse_p - max), as the general form does;
   // up to eight partitions' log-sum-exps are loaded once, eight at a time
-  const int np = kl - kf + 1;
   float lv0[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -335,27 +366,12 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
     for (int kk = kf + 8; kk <= kl; ++kk) sum += __expf(lse_at(kk) - mx);
   }
   const float inv_sum = sum > 0.f ? 1.f / sum : 0.f;
-  const float4* sp = reinterpret_cast<const float4*>(ring);
+  int j = 0;
   for (int kk = kf; kk <= kl; ++kk) {
     const float w = mx != -CUDART_INF_F ? __expf(lse_at(kk) - mx) * inv_sum : 0.f;
-    const bool own = kk == k, first = kk == kf;
-    if (!own) {
-      bool ok = true;
-      if (row == 0) {
-        if (nmrg > 0) ok = wait_or_abort(&cs->mrg_done, (nmrg - 1) & 1, cs, hdr);
-        if (ok) {
-          const uint32_t bytes = (uint32_t)(LC * H * 4);
-          fence_proxy_async_global();
-          mbar_arrive_expect_tx(&cs->mrg_full, bytes);
-          bulk_copy_g2s(ring, reinterpret_cast<const float4*>(a.part_o) + part_index(kk, slot_of(kk), lat_x0 / 4, 0, L, H),
-                        bytes, &cs->mrg_full);
-        }
-      }
-      if (!__all_sync(0xffffffffu, ok)) return false;
-      if (!wwait(&cs->mrg_full, nmrg & 1, cs, hdr)) return false;
-    }
-    // 32 columns per step, every load of the step in flight before one wait
-    if (own) {
+    const bool first = kk == kf;
+    if (kk == k) {
+      // 32 columns per step, every load of the step in flight before one wait
 #pragma unroll 1
       for (int col = 0; col < LC; col += 32) {
         uint32_t u[32], acc[32];
@@ -363,15 +379,22 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
         if (!first) tmem_ld32(tacc + col, acc);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          acc[j] = __float_as_uint(fmaf(w, __uint_as_float(u[j]) * inv, first ? 0.f : __uint_as_float(acc[j])));
+        for (int i = 0; i < 32; ++i)
+          acc[i] = __float_as_uint(fmaf(w, __uint_as_float(u[i]) * inv, first ? 0.f : __uint_as_float(acc[i])));
         tmem_st32(tacc + col, acc);
       }
-    } else {
+      tmem_st_wait();
+      continue;
+    }
+    for (int h = 0; h < 2; ++h, ++j) {
+      const int g = nmrg + j, b = g & 1;
+      if (!wwait(&cs->mrg_full[b], (g >> 1) & 1, cs, hdr)) return false;
+      const float4* sp = reinterpret_cast<const float4*>(hb + b * kHalf);
 #pragma unroll 1
-      for (int col = 0; col < LC; col += 32) {
+      for (int col = 0; col < LH; col += 32) {
         uint32_t acc[32];
-        if (!first) tmem_ld32(tacc + col, acc);
+        const uint32_t tc = tacc + h * LH + col;
+        if (!first) tmem_ld32(tc, acc);
         float4 x[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) x[i] = live ? sp[(col / 4 + i) * H + row] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -380,35 +403,20 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
         for (int i = 0; i < 8; ++i) {
           const float v[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            acc[4 * i + j] = __float_as_uint(fmaf(w, v[j], first ? 0.f : __uint_as_float(acc[4 * i + j])));
+          for (int e = 0; e < 4; ++e)
+            acc[4 * i + e] = __float_as_uint(fmaf(w, v[e], first ? 0.f : __uint_as_float(acc[4 * i + e])));
         }
-        tmem_st32(tacc + col, acc);
+        tmem_st32(tc, acc);
       }
-    }
-    tmem_st_wait();
-    if (!own) {
-      mbar_arrive(&cs->mrg_done);
-      ++nmrg;
+      tmem_st_wait();
+      mbar_arrive(&cs->mrg_done[b]);
+      if (row == 0 && j + 2 < nj) ok = issue(j + 2);
+      if (!__all_sync(0xffffffffu, ok)) return false;
     }
   }
-  // the merged row as bf16, staged row-major in the idle ring (after the last
-  // partial there has been read by every thread), then written out so that a
-  // warp's store covers 512 contiguous bytes of one output row
-  bool synced = !(nmrg > 0 && row == 0 && !wait_or_abort(&cs->mrg_done, (nmrg - 1) & 1, cs, hdr));
-  auto sync128 = [&]() {   // short waits: spin rather than suspend
-    mbar_arrive(&cs->mrg_sync);
-    bool ok = mbar_spin(&cs->mrg_sync, nsync & 1, kWaitLimitNs);
-    if (!ok) {
-      record_timeout(&cs->mrg_sync, hdr);
-      atomicOr(&hdr->status, kDeviceTimeout);
-      *reinterpret_cast<volatile int*>(&cs->abort) = 1;
-    }
-    ++nsync;
-    return __all_sync(0xffffffffu, ok);
-  };
-  if (!__all_sync(0xffffffffu, synced) || !sync128()) return false;
-  __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(ring);
+  nmrg += nj;
+  // the merged row as bf16 in this thread's staging row, then one bulk copy
+  uint8_t* srow = stg + (size_t)row * kStgStride;
 #pragma unroll 1
   for (int col = 0; col < LC; col += 32) {
     uint32_t r[32];
@@ -417,26 +425,17 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
     uint32_t o[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i] = pack_bf16(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-    // row-major [128][LC] with the 16-byte chunk index rotated by the row, so
-    // a warp's 32 rows write different banks
-    uint4* rowp = reinterpret_cast<uint4*>(stg + (size_t)row * LC);
-    const int nch = LC / 8;
+    uint4* d = reinterpret_cast<uint4*>(srow + col * 2);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      rowp[(col / 8 + i + row) % nch] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
   }
-  if (!sync128()) return false;
-  {
-    const int nch = LC / 8;                 // 16-byte chunks per row half
-    const int tid4 = row;                   // 0..127 over the four softmax warps
-    for (int idx = tid4; idx < 128 * nch; idx += 128) {
-      const int rr = idx / nch, ch = idx % nch;
-      if (rr >= H) continue;
-      const uint4 v = reinterpret_cast<const uint4*>(stg + (size_t)rr * LC)[(ch + rr) % nch];
-      reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + rr) * L + lat_x0)[ch] = v;
-    }
+  if (live) {
+    fence_proxy_async_smem();
+    bulk_copy_s2g(a.o_lat + ((size_t)t * H + row) * L + lat_x0, srow, LC * 2);
+    bulk_commit();
+    if (rank == 0) a.lse_ws[(size_t)t * H + row] = mx != -CUDART_INF_F ? mx + __logf(sum) : -CUDART_INF_F;
+    bulk_wait_all();
   }
-  if (live && rank == 0) a.lse_ws[(size_t)t * H + row] = mx != -CUDART_INF_F ? mx + __logf(sum) : -CUDART_INF_F;
   return true;
 }
 
@@ -489,9 +488,10 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     mbar_init(&cs->conv_sync, C::kConvThreads);
     mbar_init(&cs->fix_bar, 128);
     mbar_init(&cs->fix_done, 1);
-    mbar_init(&cs->mrg_full, 1);
-    mbar_init(&cs->mrg_done, 128);
-    mbar_init(&cs->mrg_sync, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&cs->mrg_full[i], 1);
+      mbar_init(&cs->mrg_done[i], 128);
+    }
     mbar_init(&cs->bye, 1);
     cs->abort = 0;
     fence_mbar_init();
@@ -908,8 +908,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     };
     int c = 0;
     int nfix = 0;   // split-token merges attempted (phase of fix_bar / fix_done)
-    int nmrg = 0;   // partials brought in by bulk copy (phase of mrg_full / mrg_done)
-    int nsync = 0;  // merge-wide syncs (phase of mrg_sync)
+    int nmrg = 0;   // half partials brought in by bulk copy (buffer and phase of mrg_full / mrg_done)
     bool q_ready = false;   // the coming segment's query is already in TMEM
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
                                      int next_t) {
@@ -1072,8 +1071,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       }
       if (!complete) {
         // split token: the partition that finishes it last (per cluster rank)
-        // merges every partition's partial into o_lat / lse
-        __threadfence();
+        // merges every partition's partial into o_lat / lse.  The barrier orders
+        // the 128 threads' partial rows before thread row 0, whose gpu-scope fence
+        // then publishes them all ahead of its counter increment; the merging
+        // CTA's row 0 fences again after reading the count, and its barrier
+        // arrival passes that ordering on to the other threads.
         mbar_arrive(&cs->fix_bar);
         const int Qt = (total + a.K - 1) / a.K;
         const int kf = tp.tile_start / Qt, kl = (tp.tile_start + tp.ntiles - 1) / Qt;
@@ -1081,8 +1083,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (row == 0) {
           ok0 = wait_or_abort(&cs->fix_bar, nfix & 1, cs, hdr);
           if (ok0) {
+            __threadfence();
             const int prev = atomicAdd(&a.counters[2 * t + rank], 1);
-            cs->fix_last = prev == kl - kf;
+            const bool last = prev == kl - kf;
+            if (last) __threadfence();
+            cs->fix_last = last;
             mbar_arrive(&cs->fix_done);
           }
         }
@@ -1090,12 +1095,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (!__all_sync(0xffffffffu, ok0 && ok1)) return;
         ++nfix;
         if (cs->fix_last) {
-          __threadfence();
           if (tp.tile_start + ie >= g1) {
             // This was the partition's last segment: O in TMEM still holds this
             // CTA's own partial and the stage ring is idle.
-            if (!merge_in_tmem(a, cs, t, tp, k, kf, kl, Qt, rank, row, lat_x0, LC, trow, trow + C::kSCol, lse, inv,
-                               sStage, nmrg, nsync))
+            if (!merge_in_tmem<LC>(a, cs, t, tp, k, kf, kl, Qt, rank, row, lat_x0, trow, trow + C::kSCol, lse, inv,
+                                   sQ, sQ + C::kRegionBytes - 2 * C::kMrgHalf, nmrg))
               return;
           } else if (live) {
             merge_split_token(a, t, tp, kf, kl, Qt, rank, row, lat_x0, LC);

@@ -155,6 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   asm volatile("griddepcontrol.wait;" ::: "memory");   // q (absorb) / o_lat, lse of the decode (W_uv)
   if (tid == 0)
     for (int kb = 0; kb < nkb && kb < S; ++kb) load_x(kb);
+  // W_uv: the log-sum-exp rows go out while the MMAs run (not thread 0's warp
+  // when one thread runs the k loop)
+  if (a.mode == 1 && a.lse_out && (kFp8 || warp > 0)) {
+    const int first = kFp8 ? tid : tid - 32, stride = kFp8 ? kThreads : kThreads - 32;
+    for (int j = first; j < TN; j += stride)
+      if (t0 + j < a.T) a.lse_out[(size_t)(t0 + j) * a.H + h] = a.lse_ws[(size_t)(t0 + j) * a.H + h];
+  }
 
   const uint32_t idesc = idesc_bf16_f32(128, TN, false, false);
   // MMAs of k step kb (stage s) into the accumulators, and the stage's refill
@@ -315,10 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
       for (int tt = tid >> 4; tt < ntok; tt += kThreads / 16)
         *reinterpret_cast<uint4*>(dst + tt * dst_pitch) = *reinterpret_cast<const uint4*>(src + tt * 128);
     }
-  }
-  if (a.mode == 1 && a.lse_out) {
-    for (int j = tid; j < TN; j += kThreads)
-      if (t0 + j < a.T) a.lse_out[(size_t)(t0 + j) * a.H + h] = a.lse_ws[(size_t)(t0 + j) * a.H + h];
   }
   tc_fence_before();
   __syncthreads();
