@@ -50,7 +50,8 @@ struct KeySource {
 // Byte offsets of the workspace sections:
 //   header     PlanHeader (total tiles, status word)
 //   plan       TokenPlan [T]
-//   counters   int [T, 2]: partitions that finished a split token, per cluster rank
+//   counters   int [T, 4]: per split token, partitions that claimed it / wrote their
+//              partial, each per cluster rank
 //   q_full     bf16 [T, 128, L+R]: absorbed queries, rows h >= H zero
 //   o_lat      bf16 [T, H, L]: normalised latent outputs
 //   lse        fp32 [T, H]
@@ -67,7 +68,7 @@ inline WorkspaceLayout workspace_layout(const mla_dims_t& d, int T, int K) {
   size_t o = 0;
   w.header = o;  o = up(o + sizeof(PlanHeader));
   w.plan = o;    o = up(o + sizeof(TokenPlan) * (size_t)(T > 0 ? T : 1));
-  w.counters = o; o = up(o + sizeof(int) * 2 * (size_t)(T > 0 ? T : 1));
+  w.counters = o; o = up(o + sizeof(int) * 4 * (size_t)(T > 0 ? T : 1));
   w.q_full = o;  o = up(o + (size_t)T * kMaxHeads * (d.kv_lora_rank + d.qk_rope) * 2);
   w.o_lat = o;   o = up(o + (size_t)T * d.num_heads * d.kv_lora_rank * 2);
   w.lse = o;     o = up(o + (size_t)T * d.num_heads * 4);

@@ -73,13 +73,13 @@ struct Smem {   // control block after the stage ring
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_free;
   uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
-  uint64_t fix_bar, fix_done;    // softmax: partial written / merge decision published
+  uint64_t fix_bar, fix_done;    // softmax: partial written / claim outcome published
   uint64_t mrg_full[2], mrg_done[2];   // merge: a half partial landed in its buffer / was read
   uint64_t bye;                  // the peer CTA is done touching this CTA's shared memory
   int32_t rowid[kMaxStages][64]; // physical row of each tile row (kLoadFp8, kLoadSparse)
   uint32_t tmem_base;
   int abort;
-  int fix_last;   // this CTA merges the split token it just finished
+  int fix_last;   // this CTA merges the split token it just finished (it claimed it last)
 };
 
 template <int kLatentPerCta, int kCluster, int kMode>
@@ -172,6 +172,17 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
   atomicOr(&hdr->status, kDeviceTimeout);
   *reinterpret_cast<volatile int*>(&cs->abort) = 1;
   return false;
+}
+
+// Bounded wait until the counter that other CTAs increment reaches `target`.
+__device__ __forceinline__ bool wait_count(const int* ctr, int target, uint64_t limit_ns) {
+  if (*reinterpret_cast<const volatile int*>(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(32);
+    if (*reinterpret_cast<const volatile int*>(ctr) >= target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 
 __device__ __forceinline__ bool wait_cluster_or_abort(uint64_t* bar, uint32_t parity, Smem* cs,
@@ -907,7 +918,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       return true;
     };
     int c = 0;
-    int nfix = 0;   // split-token merges attempted (phase of fix_bar / fix_done)
+    int nfix = 0;   // split-token segments ended (phase of fix_done)
+    int nbar = 0;   // split-token partials published (phase of fix_bar)
     int nmrg = 0;   // half partials brought in by bulk copy (buffer and phase of mrg_full / mrg_done)
     bool q_ready = false;   // the coming segment's query is already in TMEM
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
@@ -1029,83 +1041,118 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (!copy_q(si + 1)) return;
         q_ready = true;
       }
+      const bool complete = ia == 0 && ie == tp.ntiles;
+      const bool final_seg = tp.tile_start + ie >= g1;   // the partition's last segment
+      const int Qt = (total + a.K - 1) / a.K;
+      const int kf = tp.tile_start / Qt, kl = (tp.tile_start + tp.ntiles - 1) / Qt;
+      // Split token: every partition (per cluster rank) claims it once; the last
+      // to claim merges all partitions' partials into o_lat / lse after the
+      // others have counted theirs as written.  A partition's final segment
+      // claims before its last P . C completes, so that if it merges, its own
+      // partial never leaves TMEM; an earlier segment writes first and claims
+      // after (its O must be read out for the next segment anyway).  A claimer
+      // that does not merge depends on nothing outside its CTA from the claim
+      // to its written count, so the merger's wait ends.
+      const bool early_claim = !complete && final_seg;
+      int claim = 0;
+      if (early_claim && row == 0) claim = atomicAdd(&a.counters[4 * t + rank], 1);
       if (!wwait(&cs->pv_done[last_c & 1], (last_c >> 1) & 1, cs, hdr)) return;
       tc_fence_after();
-      const bool complete = ia == 0 && ie == tp.ntiles;
+      // row 0 of a merger: wait for the other partitions' written partials
+      auto await_written = [&]() {
+        if (wait_count(&a.counters[4 * t + 2 + rank], kl - kf, kWaitLimitNs)) {
+          __threadfence();
+          return true;
+        }
+        record_timeout(&cs->fix_done, hdr);
+        atomicOr(&hdr->status, kDeviceTimeout);
+        *reinterpret_cast<volatile int*>(&cs->abort) = 1;
+        return false;
+      };
+      bool merger = false;
+      if (early_claim) {
+        if (row == 0) {
+          cs->fix_last = claim == kl - kf && await_written();
+          mbar_arrive(&cs->fix_done);
+        }
+        if (!wwait(&cs->fix_done, nfix & 1, cs, hdr) || waborted(cs)) return;
+        ++nfix;
+        merger = cs->fix_last;
+      }
       const int slot = is_first_seg ? 0 : 1;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
       const bool live = row < H;
+      if (!merger) {
 #pragma unroll 1
-      for (int col = 0; col < LC; col += 32) {
-        uint32_t r[32];
-        tmem_ld32(trow + col, r);
-        tmem_ld_wait();
-        if (!live) continue;
-        if (complete) {
-          uint32_t o[16];
+        for (int col = 0; col < LC; col += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + col, r);
+          tmem_ld_wait();
+          if (!live) continue;
+          if (complete) {
+            uint32_t o[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            o[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + row) * L + lat_x0 + col);
+            for (int i = 0; i < 16; ++i)
+              o[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+            uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)t * H + row) * L + lat_x0 + col);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-        } else {
-          float4* po = reinterpret_cast<float4*>(a.part_o);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          } else {
+            float4* po = reinterpret_cast<float4*>(a.part_o);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            po[part_index(k, slot, (lat_x0 + col) / 4 + i, row, L, H)] =
-                make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
-                            __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+            for (int i = 0; i < 8; ++i)
+              po[part_index(k, slot, (lat_x0 + col) / 4 + i, row, L, H)] =
+                  make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                              __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+          }
+        }
+        if (live) {
+          if (complete) {
+            if (rank == 0) a.lse_ws[(size_t)t * H + row] = lse;
+          } else {
+            a.part_lse[((size_t)(k * 2 + slot) * 2 + rank) * H + row] = lse;
+          }
         }
       }
       // O has been read: the next segment's first P . C may overwrite it
       tc_fence_before();
       mbar_arrive(&cs->o_free);
-      if (live) {
-        if (complete) {
-          if (rank == 0) a.lse_ws[(size_t)t * H + row] = lse;
-        } else {
-          a.part_lse[((size_t)(k * 2 + slot) * 2 + rank) * H + row] = lse;
-        }
-      }
-      if (!complete) {
-        // split token: the partition that finishes it last (per cluster rank)
-        // merges every partition's partial into o_lat / lse.  The barrier orders
-        // the 128 threads' partial rows before thread row 0, whose gpu-scope fence
-        // then publishes them all ahead of its counter increment; the merging
-        // CTA's row 0 fences again after reading the count, and its barrier
-        // arrival passes that ordering on to the other threads.
+      if (complete) return;
+      if (merger) {
+        // the partition's final segment: O in TMEM still holds this CTA's own
+        // partial and the query buffer and stage ring are idle
+        if (!merge_in_tmem<LC>(a, cs, t, tp, k, kf, kl, Qt, rank, row, lat_x0, trow, trow + C::kSCol, lse, inv, sQ,
+                               sQ + C::kRegionBytes - 2 * C::kMrgHalf, nmrg))
+          return;
+      } else {
+        // publish the partial: the barrier orders the 128 threads' rows before
+        // thread row 0, whose gpu-scope fence covers them all ahead of its count
         mbar_arrive(&cs->fix_bar);
-        const int Qt = (total + a.K - 1) / a.K;
-        const int kf = tp.tile_start / Qt, kl = (tp.tile_start + tp.ntiles - 1) / Qt;
-        bool ok0 = true;
         if (row == 0) {
-          ok0 = wait_or_abort(&cs->fix_bar, nfix & 1, cs, hdr);
-          if (ok0) {
+          bool last = false;
+          if (wait_or_abort(&cs->fix_bar, nbar & 1, cs, hdr)) {
             __threadfence();
-            const int prev = atomicAdd(&a.counters[2 * t + rank], 1);
-            const bool last = prev == kl - kf;
-            if (last) __threadfence();
-            cs->fix_last = last;
-            mbar_arrive(&cs->fix_done);
+            if (!early_claim) last = atomicAdd(&a.counters[4 * t + rank], 1) == kl - kf;
+            if (last) last = await_written();
+            else atomicAdd(&a.counters[4 * t + 2 + rank], 1);
           }
+          cs->fix_last = last;
+          if (!early_claim) mbar_arrive(&cs->fix_done);
         }
-        const bool ok1 = wait_or_abort(&cs->fix_done, nfix & 1, cs, hdr);
-        if (!__all_sync(0xffffffffu, ok0 && ok1)) return;
+        ++nbar;
+        __syncwarp();
+        if (early_claim) return;
+        if (!wwait(&cs->fix_done, nfix & 1, cs, hdr) || waborted(cs)) return;
         ++nfix;
-        if (cs->fix_last) {
-          if (tp.tile_start + ie >= g1) {
-            // This was the partition's last segment: O in TMEM still holds this
-            // CTA's own partial and the stage ring is idle.
-            if (!merge_in_tmem<LC>(a, cs, t, tp, k, kf, kl, Qt, rank, row, lat_x0, trow, trow + C::kSCol, lse, inv,
-                                   sQ, sQ + C::kRegionBytes - 2 * C::kMrgHalf, nmrg))
-              return;
-          } else if (live) {
-            merge_split_token(a, t, tp, kf, kl, Qt, rank, row, lat_x0, LC);
-          }
-          if (row == 0) a.counters[2 * t + rank] = 0;
-        }
+        if (!cs->fix_last) return;
+        // a merger in an earlier segment: every partial, its own included, is in
+        // global memory (its own rows were written by these same threads)
+        if (live) merge_split_token(a, t, tp, kf, kl, Qt, rank, row, lat_x0, LC);
+      }
+      if (row == 0) {
+        a.counters[4 * t + rank] = 0;
+        a.counters[4 * t + 2 + rank] = 0;
       }
     });
   }

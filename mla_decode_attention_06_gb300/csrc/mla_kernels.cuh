@@ -25,7 +25,7 @@ struct DecodeArgs {
   float* lse_ws;                // [T, H]
   float* part_o;                // [K, 2, H, L]
   float* part_lse;              // [K, 2, 2, H]
-  int* counters;                // [T, 2]
+  int* counters;                // [T, 4]
 };
 
 

@@ -17,7 +17,7 @@ struct PlanInputs {
   int mask, window;
   TokenPlan* plan;           // [T]
   PlanHeader* hdr;
-  int* counters;             // [T, 2] split-token arrival counters, zeroed here
+  int* counters;             // [T, 4] split-token claim / written counters, zeroed here
   __nv_bfloat16* o_lat;      // [T, H, L]: zeroed for tokens without keys
   float* lse_ws;             // [T, H]:    -inf for tokens without keys
   int H, L;
@@ -104,7 +104,7 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   __syncthreads();
   const int base = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - my_tiles;
   for (int t = t0; t < t1; ++t) in.plan[t].tile_start += base;
-  for (int i = tid; i < 2 * in.T; i += nthr) in.counters[i] = 0;
+  for (int i = tid; i < 4 * in.T; i += nthr) in.counters[i] = 0;
   if (tid == nthr - 1) in.hdr->total_tiles = base + my_tiles;
   // tokens with no key: zero latent output and lse = -inf (the decode never visits
   // them); each thread clears its own tokens

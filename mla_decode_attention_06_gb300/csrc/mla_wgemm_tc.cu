@@ -60,7 +60,7 @@ struct Args {
   // W_uv
   __nv_bfloat16* out; int V; const float* lse_ws; float* lse_out;
   PlanHeader* hdr;
-  PlanInputs pin;      // absorb: block (0, 0, 0) also plans the call
+  PlanInputs pin;      // absorb: block (0, H, 0) plans the call
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, PlanHeader* hdr) {
@@ -105,8 +105,12 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, t0 = blockIdx.z * TN;
-  // absorb: the first block also plans the call (first, so it overlaps the other blocks' GEMMs)
-  if (a.mode == 0 && h == 0 && blockIdx.z == 0) plan_block(a.pin);
+  // absorb: one block of its own plans the call, beside the GEMM blocks (the
+  // decode reads the plan after this grid completes)
+  if (a.mode == 0 && h == a.H) {
+    if (blockIdx.z == 0) plan_block(a.pin);
+    return;
+  }
   const int nkb = (a.K + 63) / 64;                 // 64-wide k steps
   const int nacc = kFp8 ? (a.K + 127) / 128 : 1;   // accumulators per weight block
   const int ncols_needed = MB * nacc * TN;
@@ -427,7 +431,7 @@ cudaError_t launch(const Args& a0, WFmt wf, const void* w, const void* x, int Kx
   const size_t ring_bytes = std::max((size_t)a.S * stage_smem, (size_t)a.MB * a.TN * 128 * 2);
   const size_t smem = 1024 + ring_bytes + (2 * kMaxStages + 2) * 8;
   if (smem > 232448) return cudaErrorInvalidValue;
-  dim3 grid(1, a.H, (a.T + a.TN - 1) / a.TN);
+  dim3 grid(1, a.H + (a.mode == 0 ? 1 : 0), (a.T + a.TN - 1) / a.TN);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
