@@ -146,6 +146,7 @@ int run(const CallCommon& c) {
   a.part_o = reinterpret_cast<float*>(ws + lay.part_o);
   a.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   a.counters = reinterpret_cast<int*>(ws + lay.counters);
+  a.bounds = reinterpret_cast<const int*>(ws + lay.bounds);
   PlanInputs pin{};
   pin.offsets = c.offsets;
   pin.B = c.B;
@@ -156,6 +157,8 @@ int run(const CallCommon& c) {
   pin.plan = plan;
   pin.hdr = hdr;
   pin.counters = a.counters;
+  pin.bounds = reinterpret_cast<int*>(ws + lay.bounds);
+  pin.K = K;
   pin.o_lat = a.o_lat;
   pin.lse_ws = a.lse_ws;
   pin.H = c.d->num_heads;

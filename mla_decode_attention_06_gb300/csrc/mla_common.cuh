@@ -26,7 +26,7 @@ struct TokenPlan {
   int32_t tile_first;
   int32_t tile_start;
   int32_t ntiles;
-  int32_t pad[2];
+  int32_t part_first, part_last;   // the KV partitions holding its first / last tile
 };
 
 struct PlanHeader {
@@ -52,13 +52,14 @@ struct KeySource {
 //   plan       TokenPlan [T]
 //   counters   int [T, 4]: per split token, partitions that claimed it / wrote their
 //              partial, each per cluster rank
+//   bounds     int [K + 1]: first global tile of each KV partition, then the total
 //   q_full     bf16 [T, 128, L+R]: absorbed queries, rows h >= H zero
 //   o_lat      bf16 [T, H, L]: normalised latent outputs
 //   lse        fp32 [T, H]
 //   part_o     fp32 [K, 2, H, L]: partials of the first / last segment of each partition
 //   part_lse   fp32 [K, 2, 2, H]: their log-sum-exp, one copy per cluster rank
 struct WorkspaceLayout {
-  size_t header, plan, counters, q_full, o_lat, lse, part_o, part_lse, total;
+  size_t header, plan, counters, bounds, q_full, o_lat, lse, part_o, part_lse, total;
 };
 
 // Host-side: the layout for T tokens and K KV partitions.
@@ -69,6 +70,7 @@ inline WorkspaceLayout workspace_layout(const mla_dims_t& d, int T, int K) {
   w.header = o;  o = up(o + sizeof(PlanHeader));
   w.plan = o;    o = up(o + sizeof(TokenPlan) * (size_t)(T > 0 ? T : 1));
   w.counters = o; o = up(o + sizeof(int) * 4 * (size_t)(T > 0 ? T : 1));
+  w.bounds = o;  o = up(o + sizeof(int) * ((size_t)K + 1));
   w.q_full = o;  o = up(o + (size_t)T * kMaxHeads * (d.kv_lora_rank + d.qk_rope) * 2);
   w.o_lat = o;   o = up(o + (size_t)T * d.num_heads * d.kv_lora_rank * 2);
   w.lse = o;     o = up(o + (size_t)T * d.num_heads * 4);
@@ -88,12 +90,14 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
   return __half2float(__half(h));
 }
 
-// First global tile of the work partition k when `total` tiles are split in K parts.
-__device__ __forceinline__ int partition_begin(int k, int K, int total) {
-  int q = (total + K - 1) / K;
-  int v = k * q;
-  return v < total ? v : total;
-}
+// Partition bounds when the plan balances by cost: a token costs
+// kTileCost per tile plus kSegmentCost for the segment it starts (reading out
+// and writing its output or partial, switching the query: about 2.5 tiles of
+// decode time).  Balancing applies when every partition gets at least
+// kMinPartitionCost, which keeps consecutive bounds at least two tiles apart.
+constexpr int kTileCost = 8;
+constexpr int kSegmentCost = 20;
+constexpr int kMinPartitionCost = 40;
 
 // Token whose global tile interval contains tile g (tokens with no tiles are skipped).
 __device__ __forceinline__ int token_of_tile(const TokenPlan* plan, int T, int g) {

@@ -1,9 +1,10 @@
 // K2 (tensor-core version): split-KV MLA decode on tcgen05 with TMEM accumulators.
 //
-// Work split: partition k of K owns the global 64-key tiles [k*Q, (k+1)*Q)
-// (Q = ceil(total/K)); it walks them as segments, one per query token it
+// Work split: partition k of K owns the global 64-key tiles [bounds[k],
+// bounds[k+1]), which the plan sets for equal cost (tiles plus a charge per
+// token it starts); it walks them as segments, one per query token it
 // touches, and writes either the finished latent output (segment = whole
-// token) or a partial (o_p, lse_p) that the last partition to finish the token
+// token) or a partial (o_p, lse_p) that the last partition to claim the token
 // merges.  These are the split-KV partitions behind num_partitions_in on the
 // generic_flare_mla_decode_kv_cache_ragged page.
 //
@@ -249,11 +250,11 @@ __device__ __forceinline__ size_t part_index(int k, int slot, int c, int row, in
 // (the merging CTA's own partial still in TMEM, its stage ring idle) runs in
 // the softmax epilogue instead.
 __device__ __noinline__ void merge_split_token(const DecodeArgs& a, int t, const TokenPlan& tp, int kf, int kl,
-                                               int Qt, uint32_t rank, int row, int lat_x0, int LC) {
+                                               int slot_kf, uint32_t rank, int row, int lat_x0, int LC) {
   const int H = a.d.num_heads, L = a.d.kv_lora_rank;
   const float4* __restrict__ part_o = reinterpret_cast<const float4*>(a.part_o);
   const float* __restrict__ part_lse = a.part_lse;
-  auto slot_of = [&](int k) { return (k == kf && tp.tile_start != k * Qt) ? 1 : 0; };
+  auto slot_of = [&](int k) { return k == kf ? slot_kf : 0; };
   auto lse_of = [&](int k) { return __ldcg(part_lse + ((size_t)(k * 2 + slot_of(k)) * 2 + rank) * H + row); };
   float mx = -CUDART_INF_F;
   for (int k = kf; k <= kl; ++k) mx = fmaxf(mx, lse_of(k));
@@ -316,7 +317,7 @@ __device__ __forceinline__ bool waborted(const Smem* cs) { return __any_sync(0xf
 // Warp-uniform; false on a time-out.
 template <int LC>
 __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t, const TokenPlan& tp, int k, int kf,
-                                           int kl, int Qt, uint32_t rank, int row, int lat_x0, uint32_t trow,
+                                           int kl, int slot_kf, uint32_t rank, int row, int lat_x0, uint32_t trow,
                                            uint32_t tacc, float lse_own, float inv, uint8_t* stg, uint8_t* hb,
                                            int& nmrg) {
   constexpr int LH = LC / 2;                            // columns per half slice
@@ -325,7 +326,7 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
   const int H = a.d.num_heads, L = a.d.kv_lora_rank;
   PlanHeader* hdr = a.hdr_mut;
   const bool live = row < H;
-  auto slot_of = [&](int kk) { return (kk == kf && tp.tile_start != kk * Qt) ? 1 : 0; };
+  auto slot_of = [&](int kk) { return kk == kf ? slot_kf : 0; };
   auto lse_ptr = [&](int kk) { return a.part_lse + ((size_t)(kk * 2 + slot_of(kk)) * 2 + rank) * H + row; };
   const int np = kl - kf + 1;
   const int nj = 2 * (np - 1);                          // half slices to bring in
@@ -526,8 +527,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   griddep_launch_dependents();
   griddep_wait();
 
-  const int total = a.hdr->total_tiles;
-  const int g0 = partition_begin(k, a.K, total), g1 = partition_begin(k + 1, a.K, total);
+  const int g0 = a.bounds[k], g1 = a.bounds[k + 1];
   const int ps = a.ks.page_size;
   const int rows_per_load = ps < kTileKeys ? ps : kTileKeys;
 
@@ -615,8 +615,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           // finishes the token last it merges the later partitions' partials
           // (written long ago, by their first segments); bring this CTA's slices
           // of them into L2 now (one lane per partition)
-          const int Qt = (total + a.K - 1) / a.K;
-          const int kl = (tp.tile_start + tp.ntiles - 1) / Qt;
+          const int kl = tp.part_last;
           const int L4 = L / 4, Hh = a.d.num_heads;
           for (int kk = k + 1 + lane; kk <= kl; kk += 32) {
             bulk_prefetch_l2(reinterpret_cast<const float4*>(a.part_o) + ((size_t)(kk * 2) * L4 + lat_x0 / 4) * Hh,
@@ -750,7 +749,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       nseg = si + 1;
       if (waborted(cs)) return;
-      if (!wwait(&cs->q_full, si & 1, cs, hdr)) return;
+      // the query's TMEM part is in place before its shared-memory part lands
+      // (that load reuses the staging buffer): the segment's first QK issues its
+      // TMEM-operand MMAs in between
+      if (!wwait(&cs->qa_done, si & 1, cs, hdr)) return;
+      bool q_smem = false;
       for (int it = ia; it < ie; ++it, ++cq) {
         if (waborted(cs)) return;
         const int s = cq % S, b = cq & 1;
@@ -791,6 +794,14 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
               mma_ts(sd, tmem + C::kQCol + 8 * (4 * j + kk), dkj + (uint64_t)((kk * 32) >> 4), idesc_qk,
                      (j > 0 || kk > 0) ? 1u : 0u);
           }
+        }
+        if (!q_smem) {
+          __syncwarp();
+          if (!wwait(&cs->q_full, si & 1, cs, hdr)) return;
+          tc_fence_after();
+          q_smem = true;
+        }
+        if (lane == 0) {
 #pragma unroll 1
           for (int i = 0; i <= C::NQS; ++i) {
             // box i of the query buffer pairs with cache box QT / 64 + i (the rope box after the latent ones)
@@ -920,6 +931,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     int c = 0;
     int nfix = 0;   // split-token segments ended (phase of fix_done)
     int nbar = 0;   // split-token partials published (phase of fix_bar)
+    int pend_t = -1, pend_claim = -1;   // a split token of an earlier segment, its claim (row 0)
+    TokenPlan pend_tp{};
     int nmrg = 0;   // half partials brought in by bulk copy (buffer and phase of mrg_full / mrg_done)
     bool q_ready = false;   // the coming segment's query is already in TMEM
     for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
@@ -1043,16 +1056,18 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       }
       const bool complete = ia == 0 && ie == tp.ntiles;
       const bool final_seg = tp.tile_start + ie >= g1;   // the partition's last segment
-      const int Qt = (total + a.K - 1) / a.K;
-      const int kf = tp.tile_start / Qt, kl = (tp.tile_start + tp.ntiles - 1) / Qt;
+      const int kf = tp.part_first, kl = tp.part_last;
+      // partition kf holds the token in its second slot if the token began inside its range
+      const int slot_kf = complete ? 0 : (tp.tile_start != a.bounds[kf] ? 1 : 0);
       // Split token: every partition (per cluster rank) claims it once; the last
-      // to claim merges all partitions' partials into o_lat / lse after the
-      // others have counted theirs as written.  A partition's final segment
-      // claims before its last P . C completes, so that if it merges, its own
-      // partial never leaves TMEM; an earlier segment writes first and claims
-      // after (its O must be read out for the next segment anyway).  A claimer
-      // that does not merge depends on nothing outside its CTA from the claim
-      // to its written count, so the merger's wait ends.
+      // to claim merges all partitions' partials into o_lat / lse once the
+      // partials are counted as written.  A partition's final segment claims
+      // before its last P . C completes, so that if it merges, its own partial
+      // never leaves TMEM.  An earlier segment (at most one: the partition's
+      // first) writes its partial, counts it and claims without waiting for the
+      // outcome; it is decided after the partition's final segment.  A claimer
+      // that does not merge depends on nothing outside its CTA from its claim to
+      // its written count, so a merger's wait ends.
       const bool early_claim = !complete && final_seg;
       int claim = 0;
       if (early_claim && row == 0) claim = atomicAdd(&a.counters[4 * t + rank], 1);
@@ -1122,39 +1137,60 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       if (merger) {
         // the partition's final segment: O in TMEM still holds this CTA's own
         // partial and the query buffer and stage ring are idle
-        if (!merge_in_tmem<LC>(a, cs, t, tp, k, kf, kl, Qt, rank, row, lat_x0, trow, trow + C::kSCol, lse, inv, sQ,
+        if (!merge_in_tmem<LC>(a, cs, t, tp, k, kf, kl, slot_kf, rank, row, lat_x0, trow, trow + C::kSCol, lse, inv, sQ,
                                sQ + C::kRegionBytes - 2 * C::kMrgHalf, nmrg))
           return;
-      } else {
-        // publish the partial: the barrier orders the 128 threads' rows before
-        // thread row 0, whose gpu-scope fence covers them all ahead of its count
-        mbar_arrive(&cs->fix_bar);
         if (row == 0) {
-          bool last = false;
-          if (wait_or_abort(&cs->fix_bar, nbar & 1, cs, hdr)) {
-            __threadfence();
-            if (!early_claim) last = atomicAdd(&a.counters[4 * t + rank], 1) == kl - kf;
-            if (last) last = await_written();
-            else atomicAdd(&a.counters[4 * t + 2 + rank], 1);
-          }
-          cs->fix_last = last;
-          if (!early_claim) mbar_arrive(&cs->fix_done);
+          a.counters[4 * t + rank] = 0;
+          a.counters[4 * t + 2 + rank] = 0;
         }
-        ++nbar;
-        __syncwarp();
-        if (early_claim) return;
-        if (!wwait(&cs->fix_done, nfix & 1, cs, hdr) || waborted(cs)) return;
-        ++nfix;
-        if (!cs->fix_last) return;
-        // a merger in an earlier segment: every partial, its own included, is in
-        // global memory (its own rows were written by these same threads)
-        if (live) merge_split_token(a, t, tp, kf, kl, Qt, rank, row, lat_x0, LC);
+        return;
       }
-      if (row == 0) {
-        a.counters[4 * t + rank] = 0;
-        a.counters[4 * t + 2 + rank] = 0;
+      // publish the partial: the barrier orders the 128 threads' rows before
+      // thread row 0, whose release increment covers them all
+      mbar_arrive(&cs->fix_bar);
+      if (row == 0 && wait_or_abort(&cs->fix_bar, nbar & 1, cs, hdr)) {
+        red_add_release_gpu(&a.counters[4 * t + 2 + rank], 1);
+        if (!early_claim) pend_claim = atomicAdd(&a.counters[4 * t + rank], 1);
       }
+      ++nbar;
+      if (!early_claim) {
+        // only a token's last partition holds it in an earlier segment, its first
+        if (pend_t >= 0 && row == 0) atomicOr(&hdr->status, kDeviceCheckFailed);
+        pend_t = t;
+        pend_tp = tp;
+      }
+      __syncwarp();
     });
+    if (pend_t >= 0) {
+      // the earlier segment's claim: the last claimer merges once all partials,
+      // its own included, are counted as written; every partial is in global
+      // memory (this CTA's own rows were written by these same threads)
+      const int kf = pend_tp.part_first, kl = pend_tp.part_last;
+      const int slot_kf = pend_tp.tile_start != a.bounds[kf] ? 1 : 0;
+      if (row == 0) {
+        bool last = pend_claim == kl - kf;
+        if (last) {
+          last = wait_count(&a.counters[4 * pend_t + 2 + rank], kl - kf + 1, kWaitLimitNs);
+          if (last) {
+            __threadfence();
+          } else {
+            record_timeout(&cs->fix_done, hdr);
+            atomicOr(&hdr->status, kDeviceTimeout);
+            *reinterpret_cast<volatile int*>(&cs->abort) = 1;
+          }
+        }
+        cs->fix_last = last;
+        mbar_arrive(&cs->fix_done);
+      }
+      if (wwait(&cs->fix_done, nfix & 1, cs, hdr) && !waborted(cs) && cs->fix_last) {
+        if (row < H) merge_split_token(a, pend_t, pend_tp, kf, kl, slot_kf, rank, row, lat_x0, LC);
+        if (row == 0) {
+          a.counters[4 * pend_t + rank] = 0;
+          a.counters[4 * pend_t + 2 + rank] = 0;
+        }
+      }
+    }
   }
 
   // ------------------------------------------------------------- teardown

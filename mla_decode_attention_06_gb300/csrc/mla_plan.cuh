@@ -1,5 +1,5 @@
-// Per-token key ranges and the global 64-key tile numbering that the decode's
-// KV partitions split evenly (the on-device counterpart of the packed dispatch
+// Per-token key ranges, the global 64-key tile numbering and the bounds of
+// the decode's KV partitions (the on-device counterpart of the packed dispatch
 // metadata `scalar_args_buf` and of `num_partitions_in` on the
 // generic_flare_mla_decode_kv_cache_ragged page).  Run by one thread block
 // inside the first kernel of a call.
@@ -18,6 +18,8 @@ struct PlanInputs {
   TokenPlan* plan;           // [T]
   PlanHeader* hdr;
   int* counters;             // [T, 4] split-token claim / written counters, zeroed here
+  int* bounds;               // [K + 1] partition bounds, written here
+  int K;                     // KV partitions
   __nv_bfloat16* o_lat;      // [T, H, L]: zeroed for tokens without keys
   float* lse_ws;             // [T, H]:    -inf for tokens without keys
   int H, L;
@@ -77,7 +79,7 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
     p.tile_first = hi > lo ? lo / kTileKeys : 0;
     p.ntiles = hi > lo ? (hi + kTileKeys - 1) / kTileKeys - p.tile_first : 0;
     p.tile_start = my_tiles;   // local for now
-    p.pad[0] = p.pad[1] = 0;
+    p.part_first = p.part_last = 0;
     in.plan[t] = p;
     my_tiles += p.ntiles;
   }
@@ -103,9 +105,79 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   }
   __syncthreads();
   const int base = (wid > 0 ? warp_sums[wid - 1] : 0) + incl - my_tiles;
+  const int total = warp_sums[(nthr >> 5) - 1];
   for (int t = t0; t < t1; ++t) in.plan[t].tile_start += base;
   for (int i = tid; i < 4 * in.T; i += nthr) in.counters[i] = 0;
-  if (tid == nthr - 1) in.hdr->total_tiles = base + my_tiles;
+  if (tid == nthr - 1) in.hdr->total_tiles = total;
+
+  // KV partition bounds: equal cost (tiles plus a charge per token) when every
+  // partition gets at least kMinPartitionCost, else equal tile counts.  A bound
+  // that falls in a token's charge goes to its first tile, one that falls in
+  // its tiles to the tile it reaches.
+  const int K = in.K;
+  long long my_cost = 0;
+  for (int t = t0; t < t1; ++t) {
+    const int n = in.plan[t].ntiles;
+    my_cost += (long long)kTileCost * n + (n > 0 ? kSegmentCost : 0);
+  }
+  long long cincl = my_cost;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long v = __shfl_up_sync(0xffffffffu, cincl, o);
+    if (lane >= o) cincl += v;
+  }
+  __shared__ long long cost_sums[32];
+  if (lane == 31) cost_sums[wid] = cincl;
+  __syncthreads();
+  if (wid == 0) {
+    long long v = lane < (nthr >> 5) ? cost_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    cost_sums[lane] = v;
+  }
+  __syncthreads();
+  const long long ctot = cost_sums[(nthr >> 5) - 1];
+  if (K > 1 && ctot >= (long long)kMinPartitionCost * K) {
+    long long c0 = (wid > 0 ? cost_sums[wid - 1] : 0) + cincl - my_cost;
+    for (int t = t0; t < t1; ++t) {
+      const TokenPlan& p = in.plan[t];
+      if (p.ntiles == 0) continue;
+      const long long c1 = c0 + (long long)kTileCost * p.ntiles + kSegmentCost;
+      // bounds k with c0 <= ctot * k / K < c1
+      for (int k = (int)(c0 * K / ctot); k < K; ++k) {
+        const long long bk = ctot * k / K;
+        if (bk >= c1) break;
+        if (bk < c0) continue;
+        const long long rel = bk - c0 - kSegmentCost;
+        const int into = rel <= 0 ? 0 : (int)min((long long)p.ntiles, (rel + kTileCost - 1) / kTileCost);
+        in.bounds[k] = p.tile_start + into;
+      }
+      c0 = c1;
+    }
+  } else {
+    const int q = K > 0 ? (total + K - 1) / K : 0;
+    for (int k = tid; k < K; k += nthr) in.bounds[k] = (int)min((long long)k * q, (long long)total);
+  }
+  if (tid == 0) in.bounds[K] = total;
+  __syncthreads();
+  // each token's first and last partition: the last k with bounds[k] <= tile
+  auto part_of = [&](int g) {
+    int lo = 0, hi = K - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (in.bounds[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  for (int t = t0; t < t1; ++t) {
+    TokenPlan& p = in.plan[t];
+    if (p.ntiles == 0) continue;
+    p.part_first = part_of(p.tile_start);
+    p.part_last = part_of(p.tile_start + p.ntiles - 1);
+  }
   // tokens with no key: zero latent output and lse = -inf (the decode never visits
   // them); each thread clears its own tokens
   for (int t = t0; t < t1; ++t) {
