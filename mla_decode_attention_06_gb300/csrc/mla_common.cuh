@@ -52,7 +52,8 @@ struct KeySource {
 //   plan       TokenPlan [T]
 //   counters   int [T, 4]: per split token, partitions that claimed it / wrote their
 //              partial, each per cluster rank
-//   bounds     int [K + 1]: first global tile of each KV partition, then the total
+//   bounds     int [2K + 1]: first global tile of each KV partition, then the total,
+//              then the token holding each partition's first tile
 //   q_full     bf16 [T, 128, L+R]: absorbed queries, rows h >= H zero
 //   o_lat      bf16 [T, H, L]: normalised latent outputs
 //   lse        fp32 [T, H]
@@ -70,7 +71,7 @@ inline WorkspaceLayout workspace_layout(const mla_dims_t& d, int T, int K) {
   w.header = o;  o = up(o + sizeof(PlanHeader));
   w.plan = o;    o = up(o + sizeof(TokenPlan) * (size_t)(T > 0 ? T : 1));
   w.counters = o; o = up(o + sizeof(int) * 4 * (size_t)(T > 0 ? T : 1));
-  w.bounds = o;  o = up(o + sizeof(int) * ((size_t)K + 1));
+  w.bounds = o;  o = up(o + sizeof(int) * (2 * (size_t)K + 1));
   w.q_full = o;  o = up(o + (size_t)T * kMaxHeads * (d.kv_lora_rank + d.qk_rope) * 2);
   w.o_lat = o;   o = up(o + (size_t)T * d.num_heads * d.kv_lora_rank * 2);
   w.lse = o;     o = up(o + (size_t)T * d.num_heads * 4);

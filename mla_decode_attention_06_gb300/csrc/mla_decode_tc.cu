@@ -123,17 +123,18 @@ struct Maps {
   CUtensorMap q;         // absorbed queries [T * 128, L + R], 64-column boxes
 };
 
-// Walks the segments of partition k: calls f(si, t, plan, first_tile, end_tile,
+// Walks the segments of partition k (tiles [g0, g1), the first in token
+// t_first, as the plan recorded): calls f(si, t, plan, first_tile, end_tile,
 // is_first_segment, next_t) where next_t is the token of the following segment
 // (-1 if none).  Consecutive segments belong to consecutive tokens, so the plan
 // entry of token t + 1 is loaded when segment t starts and is ready at the
 // boundary; only a token without keys in between (they share tile_start) falls
 // back to the search.
 template <class F>
-__device__ __forceinline__ void for_each_segment(const DecodeArgs& a, int g0, int g1, F&& f) {
+__device__ __forceinline__ void for_each_segment(const DecodeArgs& a, int g0, int g1, int t_first, F&& f) {
   int g = g0;
   int si = 0;
-  int t = g0 < g1 ? token_of_tile(a.plan, a.T, g0) : 0;
+  int t = g0 < g1 ? t_first : 0;
   while (g < g1) {
     if (t < 0 || t >= a.T) {   // a plan that does not cover g: report, never loop
       atomicOr(&a.hdr_mut->status, kDeviceCheckFailed);
@@ -527,7 +528,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   griddep_launch_dependents();
   griddep_wait();
 
-  const int g0 = a.bounds[k], g1 = a.bounds[k + 1];
+  const int g0 = a.bounds[k], g1 = a.bounds[k + 1], t_first = a.bounds[a.K + 1 + k];
   const int ps = a.ks.page_size;
   const int rows_per_load = ps < kTileKeys ? ps : kTileKeys;
 
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     };
     int c = 0;
     bool bad = false;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int next_t) {
+    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int next_t) {
       bool q_pending = true;   // the query's shared-memory part goes right after the first tile
       // The next segment's absorbed query is read at this segment's end; it goes
       // into L2 a few tiles before that (earlier, the cache stream evicts it again).
@@ -547,8 +548,21 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       constexpr int kOwn = MODE == kLoadFp8 ? C::NRH / CL : C::NLB / CL;   // this CTA's boxes per load
       const int nloads = kTileKeys / rows_per_load;
       const uint64_t lmask = rows_per_load == 64 ? ~0ull : ((1ull << rows_per_load) - 1);
-      // rows j and j + 32 of tile `it`: which key / slot, and is it live?
-      auto lookup = [&](int it, bool (&v)[2], int (&rid)[2], int (&pg)[2]) {
+      // rows j and j + 32 of tile `it`: which key / slot, and is it live?  fetch
+      // only reads the page-table entries (or indices) so that several tiles'
+      // reads can be in flight at once; finish checks and decodes them.
+      auto fetch = [&](int it, int (&raw)[2]) {
+        const int key0 = (tp.tile_first + it) * kTileKeys;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int key = key0 + lane + 32 * h;
+          raw[h] = 0;
+          if (key >= tp.lo && key < tp.hi)
+            raw[h] = MODE == kLoadSparse ? a.ks.indices[(size_t)tp.b * a.ks.idx_stride + key]
+                                         : a.ks.block_table[(size_t)tp.b * a.ks.bt_stride + key / ps];
+        }
+      };
+      auto finish = [&](int it, const int (&raw)[2], bool (&v)[2], int (&rid)[2], int (&pg)[2]) {
         const int key0 = (tp.tile_first + it) * kTileKeys;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -558,7 +572,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           pg[h] = 0;
           if (ok) {
             if (MODE == kLoadSparse) {
-              const int idx = a.ks.indices[(size_t)tp.b * a.ks.idx_stride + key];
+              const int idx = raw[h];
               if (idx >= 0 && idx < a.ks.num_pages * ps) {
                 rid[h] = idx;
               } else {
@@ -566,13 +580,18 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
                 if (idx != -1) bad = true;
               }
             } else {
-              const int page = a.ks.block_table[(size_t)tp.b * a.ks.bt_stride + key / ps];
+              const int page = raw[h];
               if (page < 0 || page >= a.ks.num_pages) { ok = false; bad = true; }
               else { pg[h] = page; rid[h] = page * ps + key % ps; }
             }
           }
           v[h] = ok;
         }
+      };
+      auto lookup = [&](int it, bool (&v)[2], int (&rid)[2], int (&pg)[2]) {
+        int raw[2];
+        fetch(it, raw);
+        finish(it, raw, v, rid, pg);
       };
       // the pool row of load p of a tile, from the lane that looked up its first live row
       auto load_row = [&](int it, int p, uint64_t pm, const int (&pg)[2]) {
@@ -585,11 +604,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       };
       // L2 prefetch of this CTA's boxes of tile `it` (paged modes): its load, issued
       // when a stage frees up, then reads L2 instead of waiting on HBM
-      auto prefetch = [&](int it) {
+      auto prefetch_from = [&](int it, const bool (&v)[2], const int (&pg)[2]) {
         if (MODE == kLoadSparse || it >= ie) return;
-        bool v[2];
-        int rid[2], pg[2];
-        lookup(it, v, rid, pg);
         const uint64_t mask = (uint64_t)__ballot_sync(0xffffffffu, v[0]) |
                               ((uint64_t)__ballot_sync(0xffffffffu, v[1]) << 32);
         for (int p = 0; p < nloads; ++p) {
@@ -604,7 +620,26 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           }
         }
       };
-      if (ia + 1 < ie) prefetch(ia + 1);
+      auto issue_qa = [&]() {   // the query's TMEM part (latent [0, QT)) into the staging buffer
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&cs->qa_full, (C::QT / 64) * C::kQBox);
+          for (int i = 0; i < C::QT / 64; ++i)
+            tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->qa_full, 64 * i, t * kMaxHeads);
+        }
+        __syncwarp();
+      };
+      // the partition's first query goes out before any page-table read: the
+      // first QK waits on it, not on the cache
+      const bool qa_sent = si == 0;
+      if (qa_sent) issue_qa();
+      if (si > 0 && MODE != kLoadSparse && ia + 1 < ie) {
+        // a later segment waits for a free stage first: bring its second tile
+        // into L2 meanwhile
+        bool v1[2];
+        int rid1[2], pg1[2];
+        lookup(ia + 1, v1, rid1, pg1);
+        prefetch_from(ia + 1, v1, pg1);
+      }
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
         const int s = c % S;
@@ -623,12 +658,18 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             bulk_prefetch_l2(a.part_lse + (size_t)(kk * 2) * 2 * Hh, (uint32_t)(2 * Hh * 4));
           }
         }
-        // global reads, issued before the wait for the stage so their latency overlaps it
-        bool v[2];
-        int rid[2], pg[2];
-        lookup(it, v, rid, pg);
+        // global reads of this tile and of the one two ahead (its L2 prefetch),
+        // issued together before the wait for the stage so their latency overlaps it
+        int raw[2], raw2[2];
+        fetch(it, raw);
+        const bool pf = MODE != kLoadSparse && it + 2 < ie;
+        if (pf) fetch(it + 2, raw2);
         // stage s is free in both CTAs once both have committed their P . C of its last tile
         if (c >= S && !wwait(&cs->kv_empty[s], ((c / S) & 1) ^ 1, cs, hdr)) return;
+        bool v[2], v2[2];
+        int rid[2], pg[2], rid2[2], pg2[2];
+        finish(it, raw, v, rid, pg);
+        if (pf) finish(it + 2, raw2, v2, rid2, pg2);
         if (MODE != kLoadDense) {
           cs->rowid[s][lane] = rid[0];
           cs->rowid[s][lane + 32] = rid[1];
@@ -698,7 +739,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
               load_box(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y);
             }
           }
-          prefetch(it + 2);
+          if (pf) prefetch_from(it + 2, v2, pg2);
         }
         __syncwarp();
         if (q_pending) {
@@ -706,13 +747,10 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           // TMEM part (latent [0, QT)) comes in through the shared-memory buffer
           // first: TMA, then the softmax threads copy their rows into TMEM; then
           // the buffer takes the shared-memory part (latent [QT, L) and rope).
-          if (si > 0 && !wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&cs->qa_full, (C::QT / 64) * C::kQBox);
-            for (int i = 0; i < C::QT / 64; ++i)
-              tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->qa_full, 64 * i, t * kMaxHeads);
+          if (!qa_sent) {
+            if (!wwait(&cs->q_empty, (si - 1) & 1, cs, hdr)) return;
+            issue_qa();
           }
-          __syncwarp();
           if (!wwait(&cs->qa_done, si & 1, cs, hdr)) return;
           if (lane == 0) {
             mbar_arrive_expect_tx(&cs->q_full, C::kQBytes);
@@ -746,7 +784,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSw128);
     const uint64_t dk0 = smem_desc(smem_u32(sStage), 16, 1024, kLayoutSw128);
     int cq = 0, nseg = 0;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
+    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       nseg = si + 1;
       if (waborted(cs)) return;
       // the query's TMEM part is in place before its shared-memory part lands
@@ -829,7 +867,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const uint32_t idesc_pv = idesc_bf16_f32(128, LC, false, true);
     const uint64_t dv0 = smem_desc(smem_u32(sStage) + (lat_x0 / 64) * C::kBox, C::kBox, 1024, kLayoutSw128);
     int cp = 0;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
+    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++cp) {
         if (waborted(cs)) return;
         const int b = cp & 1;
@@ -859,7 +897,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     // wait until every thread has read its codes.
     const int ci = tid - 192, crow = ci & 63, h = ci >> 6;
     int c = 0;
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
+    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
         const int s = c % S;
@@ -935,7 +973,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     TokenPlan pend_tp{};
     int nmrg = 0;   // half partials brought in by bulk copy (buffer and phase of mrg_full / mrg_done)
     bool q_ready = false;   // the coming segment's query is already in TMEM
-    for_each_segment(a, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
+    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
                                      int next_t) {
       if (waborted(cs)) return;
       if (!q_ready && !copy_q(si)) return;

@@ -26,7 +26,7 @@ struct DecodeArgs {
   float* part_o;                // [K, 2, H, L]
   float* part_lse;              // [K, 2, 2, H]
   int* counters;                // [T, 4]
-  const int* bounds;            // [K + 1] first global tile of each partition, then the total
+  const int* bounds;            // [2K + 1] first global tile of each partition, the total, first tokens
 };
 
 

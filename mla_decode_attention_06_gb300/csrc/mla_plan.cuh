@@ -18,7 +18,7 @@ struct PlanInputs {
   TokenPlan* plan;           // [T]
   PlanHeader* hdr;
   int* counters;             // [T, 4] split-token claim / written counters, zeroed here
-  int* bounds;               // [K + 1] partition bounds, written here
+  int* bounds;               // [2K + 1] partition bounds, then each partition's first token, written here
   int K;                     // KV partitions
   __nv_bfloat16* o_lat;      // [T, H, L]: zeroed for tokens without keys
   float* lse_ws;             // [T, H]:    -inf for tokens without keys
@@ -163,6 +163,8 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   }
   if (tid == 0) in.bounds[K] = total;
   __syncthreads();
+  for (int k = tid; k < K; k += nthr)
+    in.bounds[K + 1 + k] = in.bounds[k] < total ? token_of_tile(in.plan, in.T, in.bounds[k]) : 0;
   // each token's first and last partition: the last k with bounds[k] <= tile
   auto part_of = [&](int g) {
     int lo = 0, hi = K - 1;
