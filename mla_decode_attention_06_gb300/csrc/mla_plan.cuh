@@ -140,46 +140,57 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   }
   __syncthreads();
   const long long ctot = cost_sums[(nthr >> 5) - 1];
-  if (K > 1 && ctot >= (long long)kMinPartitionCost * K) {
-    long long c0 = (wid > 0 ? cost_sums[wid - 1] : 0) + cincl - my_cost;
-    for (int t = t0; t < t1; ++t) {
-      const TokenPlan& p = in.plan[t];
-      if (p.ntiles == 0) continue;
-      const long long c1 = c0 + (long long)kTileCost * p.ntiles + kSegmentCost;
-      // bounds k with c0 <= ctot * k / K < c1
+  // Each thread sets the bounds that fall inside its own tokens, with the token
+  // that holds each partition's first tile, and each token's first and last
+  // partition: no search over global memory.
+  const bool balanced = K > 1 && ctot >= (long long)kMinPartitionCost * K;
+  const int q = K > 0 ? (total + K - 1) / K : 0;   // tiles per partition when not balanced
+  int* first_token = in.bounds + K + 1;
+  long long c0 = (wid > 0 ? cost_sums[wid - 1] : 0) + cincl - my_cost;
+  for (int t = t0; t < t1; ++t) {
+    TokenPlan& p = in.plan[t];
+    if (p.ntiles == 0) continue;
+    const int n = p.ntiles;
+    const long long c1 = c0 + (long long)kTileCost * n + kSegmentCost;
+    if (balanced) {
+      // bounds k with c0 <= ctot * k / K < c1: past the token's charge, to the
+      // tile the cost reaches (at most its last tile, so the token holds it)
       for (int k = (int)(c0 * K / ctot); k < K; ++k) {
         const long long bk = ctot * k / K;
         if (bk >= c1) break;
         if (bk < c0) continue;
         const long long rel = bk - c0 - kSegmentCost;
-        const int into = rel <= 0 ? 0 : (int)min((long long)p.ntiles, (rel + kTileCost - 1) / kTileCost);
+        const int into = rel <= 0 ? 0 : (int)min((long long)(n - 1), (rel + kTileCost - 1) / kTileCost);
         in.bounds[k] = p.tile_start + into;
+        first_token[k] = t;
       }
-      c0 = c1;
+      // tile j of the token lies in the last partition whose bound is at or
+      // before it: the last k with ctot * k / K <= x(j), where x(j) is the cost
+      // up to tile j (the whole token for its last tile)
+      auto part_at = [&](int j) {
+        const long long x = j == n - 1 ? c1 - 1 : c0 + kSegmentCost + (long long)kTileCost * j;
+        return (int)min((long long)(K - 1), ((x + 1) * K - 1) / ctot);
+      };
+      p.part_first = part_at(0);
+      p.part_last = part_at(n - 1);
+    } else {
+      for (int k = (p.tile_start + q - 1) / q; k < K && (long long)k * q < p.tile_start + n; ++k) {
+        in.bounds[k] = k * q;
+        first_token[k] = t;
+      }
+      p.part_first = min(K - 1, p.tile_start / q);
+      p.part_last = min(K - 1, (p.tile_start + n - 1) / q);
     }
-  } else {
-    const int q = K > 0 ? (total + K - 1) / K : 0;
-    for (int k = tid; k < K; k += nthr) in.bounds[k] = (int)min((long long)k * q, (long long)total);
+    c0 = c1;
   }
+  // partitions past the last tile (tile counts below K) are empty
+  for (int k = tid; k < K; k += nthr)
+    if (!balanced && (long long)k * q >= total) {
+      in.bounds[k] = total;
+      first_token[k] = 0;
+    }
   if (tid == 0) in.bounds[K] = total;
   __syncthreads();
-  for (int k = tid; k < K; k += nthr)
-    in.bounds[K + 1 + k] = in.bounds[k] < total ? token_of_tile(in.plan, in.T, in.bounds[k]) : 0;
-  // each token's first and last partition: the last k with bounds[k] <= tile
-  auto part_of = [&](int g) {
-    int lo = 0, hi = K - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (in.bounds[mid] <= g) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-  };
-  for (int t = t0; t < t1; ++t) {
-    TokenPlan& p = in.plan[t];
-    if (p.ntiles == 0) continue;
-    p.part_first = part_of(p.tile_start);
-    p.part_last = part_of(p.tile_start + p.ntiles - 1);
-  }
   // tokens with no key: zero latent output and lse = -inf (the decode never visits
   // them); each thread clears its own tokens
   for (int t = t0; t < t1; ++t) {

@@ -9,12 +9,13 @@
 //                   m block also copy q_rope into q_full[t, h, L:L+R].
 //   W_uv   (K3): W = w_uv, m = v column, k = latent column, X = o_lat
 //                -> written as bf16 into out[t, h, v] (and lse copied out).
-// One CTA owns one head and up to 128 tokens: all M rows of the head's weight
-// (MB blocks of 128, M <= 512), N = tokens, K streamed in 64-column steps.  A
-// step loads the MB weight boxes and one activation box; the ring is as deep
-// as shared memory allows (the absorb holds all of K = 128, W_uv all of
-// K = 512 in 8 stages), so every load of the CTA is in flight at once and one
-// wave of CTAs (one per head) covers the GEMM.  The weights are read once per
+// One CTA owns one head (or half of its rows, when they split evenly into
+// 128-row blocks: two CTAs per head, two per SM) and up to 128 tokens: MB
+// blocks of 128 weight rows (M <= 512), N = tokens, K streamed in 64-column
+// steps.  A step loads the MB weight boxes and one activation box; the ring is
+// as deep as shared memory allows (the absorb holds all of K = 128, W_uv all
+// of K = 512 in 8 stages), so every load of the CTA is in flight at once and
+// one wave of CTAs covers the GEMM.  The weights are read once per
 // token block, which is what bounds these kernels (HBM): 16.8 MB per weight at
 // the DeepSeek-V3 shapes.
 //
@@ -54,13 +55,14 @@ struct Args {
   int H, T, M, K;      // heads, tokens, weight rows per head, contraction length
   int TN;              // tokens per CTA (multiple of 16, <= 128)
   int MB, S;           // weight row blocks per CTA, ring stages
+  int MC;              // CTAs per head: CTA mc of head h owns row blocks [mc * MB, mc * MB + MB)
   const float* wscale; // e4m3 block scales [H, ceil(M/128), ceil(K/128)]
   // absorb
   __nv_bfloat16* q_full; int KQ, L, R, N; const __nv_bfloat16* q;
   // W_uv
   __nv_bfloat16* out; int V; const float* lse_ws; float* lse_out;
   PlanHeader* hdr;
-  PlanInputs pin;      // absorb: block (0, H, 0) plans the call
+  PlanInputs pin;      // absorb: block (0, H * MC, 0) plans the call
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, PlanHeader* hdr) {
@@ -104,10 +106,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   auto w8_box = [&](int s, int i) { return sm + s * stage_smem + MB * kABytes + kBBytes + i * kA8Bytes; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, t0 = blockIdx.z * TN;
+  const int h = blockIdx.y / a.MC, mb0 = (blockIdx.y % a.MC) * MB, t0 = blockIdx.z * TN;
   // absorb: one block of its own plans the call, beside the GEMM blocks (the
   // decode reads the plan after this grid completes)
-  if (a.mode == 0 && h == a.H) {
+  if (a.mode == 0 && (int)blockIdx.y == a.H * a.MC) {
     if (blockIdx.z == 0) plan_block(a.pin);
     return;
   }
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   auto load_w = [&](int kb) {
     const int s = kb % S;
     for (int i = 0; i < MB; ++i)
-      tma_load_2d(kFp8 ? w8_box(s, i) : w_box(s, i), &maps.w, &full[s], kb * 64, h * a.M + 128 * i);
+      tma_load_2d(kFp8 ? w8_box(s, i) : w_box(s, i), &maps.w, &full[s], kb * 64, h * a.M + 128 * (mb0 + i));
   };
   auto load_x = [&](int kb) {
     const int s = kb % S;
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     for (int kb = 0; kb < nkb && kb < S; ++kb) load_x(kb);
   // W_uv: the log-sum-exp rows go out while the MMAs run (not thread 0's warp
   // when one thread runs the k loop)
-  if (a.mode == 1 && a.lse_out && (kFp8 || warp > 0)) {
+  if (a.mode == 1 && a.lse_out && mb0 == 0 && (kFp8 || warp > 0)) {
     const int first = kFp8 ? tid : tid - 32, stride = kFp8 ? kThreads : kThreads - 32;
     for (int j = first; j < TN; j += stride)
       if (t0 + j < a.T) a.lse_out[(size_t)(t0 + j) * a.H + h] = a.lse_ws[(size_t)(t0 + j) * a.H + h];
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   bool ok = true;
   if (!kFp8) {
     // one thread runs the whole k loop; the others only wait for the result
-    if (a.mode == 0 && warp > 0) copy_rope(tid - 32, kThreads - 32);
+    if (a.mode == 0 && mb0 == 0 && warp > 0) copy_rope(tid - 32, kThreads - 32);
     if (tid == 0) {
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int s = kb % S;
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
       }
     }
   } else {
-    if (a.mode == 0) copy_rope(tid, kThreads);
+    if (a.mode == 0 && mb0 == 0) copy_rope(tid, kThreads);
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % S;
       // every thread waits; the CTA proceeds only if all saw the stage arrive
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     float sc[4] = {1.f, 1.f, 1.f, 1.f};
     if (kFp8) {
       const int nmb = (a.M + 127) / 128;
-      for (int b = 0; b < nacc && b < 4; ++b) sc[b] = a.wscale[((size_t)h * nmb + i) * nacc + b];
+      for (int b = 0; b < nacc && b < 4; ++b) sc[b] = a.wscale[((size_t)h * nmb + mb0 + i) * nacc + b];
     }
     for (int j0 = 0; j0 < TN; j0 += 32) {
       // 32 token columns of every accumulator in flight before one wait
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     const int piece = tid & 15;
     const int ntok = min(TN, a.T - t0);
     for (int i = 0; i < MB; ++i) {
-      const int m = 128 * i + 8 * piece;
+      const int m = 128 * (mb0 + i) + 8 * piece;
       if (m >= a.M) continue;
       const __nv_bfloat16* src = stg + (size_t)i * TN * 128 + 8 * piece;
       __nv_bfloat16* dst = a.mode == 0 ? a.q_full + ((size_t)t0 * kMaxHeads + h) * a.KQ + m
@@ -360,6 +362,10 @@ cudaError_t launch(const Args& a0, WFmt wf, const void* w, const void* x, int Kx
   a.TN = a.T >= kMaxTokens ? kMaxTokens : ((a.T + 15) / 16) * 16;
   a.MB = (a.M + 127) / 128;
   if (a.MB > kMaxMB) return cudaErrorInvalidValue;
+  // two CTAs per head when the row blocks split evenly: twice the CTAs (two
+  // fit on an SM), half the weight bytes and output rows each
+  a.MC = a.MB % 2 == 0 ? 2 : 1;
+  a.MB /= a.MC;
   {
     // TMEM: MB weight blocks x (e4m3: one accumulator per 128-wide k block) x TN columns
     const int nacc = wf == WFmt::kE4M3 ? (a.K + 127) / 128 : 1;
@@ -431,7 +437,7 @@ cudaError_t launch(const Args& a0, WFmt wf, const void* w, const void* x, int Kx
   const size_t ring_bytes = std::max((size_t)a.S * stage_smem, (size_t)a.MB * a.TN * 128 * 2);
   const size_t smem = 1024 + ring_bytes + (2 * kMaxStages + 2) * 8;
   if (smem > 232448) return cudaErrorInvalidValue;
-  dim3 grid(1, a.H + (a.mode == 0 ? 1 : 0), (a.T + a.TN - 1) / a.TN);
+  dim3 grid(1, a.H * a.MC + (a.mode == 0 ? 1 : 0), (a.T + a.TN - 1) / a.TN);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
