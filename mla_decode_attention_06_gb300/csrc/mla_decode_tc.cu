@@ -123,18 +123,17 @@ struct Maps {
   CUtensorMap q;         // absorbed queries [T * 128, L + R], 64-column boxes
 };
 
-// Walks the segments of partition k (tiles [g0, g1), the first in token
-// t_first, as the plan recorded): calls f(si, t, plan, first_tile, end_tile,
+// Walks the segments of partition k (tiles [g0, g1)): calls f(si, t, plan, first_tile, end_tile,
 // is_first_segment, next_t) where next_t is the token of the following segment
 // (-1 if none).  Consecutive segments belong to consecutive tokens, so the plan
 // entry of token t + 1 is loaded when segment t starts and is ready at the
 // boundary; only a token without keys in between (they share tile_start) falls
 // back to the search.
 template <class F>
-__device__ __forceinline__ void for_each_segment(const DecodeArgs& a, int g0, int g1, int t_first, F&& f) {
+__device__ __forceinline__ void for_each_segment(const DecodeArgs& a, int k, int g0, int g1, F&& f) {
   int g = g0;
   int si = 0;
-  int t = g0 < g1 ? t_first : 0;
+  int t = g0 < g1 ? a.bounds[a.K + 1 + k] : 0;   // the token holding tile g0, recorded by the plan
   while (g < g1) {
     if (t < 0 || t >= a.T) {   // a plan that does not cover g: report, never loop
       atomicOr(&a.hdr_mut->status, kDeviceCheckFailed);
@@ -528,7 +527,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   griddep_launch_dependents();
   griddep_wait();
 
-  const int g0 = a.bounds[k], g1 = a.bounds[k + 1], t_first = a.bounds[a.K + 1 + k];
+  const int g0 = a.bounds[k], g1 = a.bounds[k + 1];
   const int ps = a.ks.page_size;
   const int rows_per_load = ps < kTileKeys ? ps : kTileKeys;
 
@@ -540,7 +539,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     };
     int c = 0;
     bool bad = false;
-    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int next_t) {
+    for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int next_t) {
       bool q_pending = true;   // the query's shared-memory part goes right after the first tile
       // The next segment's absorbed query is read at this segment's end; it goes
       // into L2 a few tiles before that (earlier, the cache stream evicts it again).
@@ -658,17 +657,20 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             bulk_prefetch_l2(a.part_lse + (size_t)(kk * 2) * 2 * Hh, (uint32_t)(2 * Hh * 4));
           }
         }
-        // global reads of this tile and of the one two ahead (its L2 prefetch),
-        // issued together before the wait for the stage so their latency overlaps it
+        // global reads of this tile and (bf16 pool) of the one two ahead, for its
+        // L2 prefetch, issued together before the wait for the stage so their
+        // latency overlaps it.  The e4m3 kernel, short of registers, reads the
+        // tile two ahead after issuing this one's loads instead.
         int raw[2], raw2[2];
         fetch(it, raw);
-        const bool pf = MODE != kLoadSparse && it + 2 < ie;
+        const bool pf = MODE == kLoadDense && it + 2 < ie;
         if (pf) fetch(it + 2, raw2);
-        // stage s is free in both CTAs once both have committed their P . C of its last tile
-        if (c >= S && !wwait(&cs->kv_empty[s], ((c / S) & 1) ^ 1, cs, hdr)) return;
         bool v[2], v2[2];
         int rid[2], pg[2], rid2[2], pg2[2];
-        finish(it, raw, v, rid, pg);
+        if (MODE != kLoadDense) finish(it, raw, v, rid, pg);
+        // stage s is free in both CTAs once both have committed their P . C of its last tile
+        if (c >= S && !wwait(&cs->kv_empty[s], ((c / S) & 1) ^ 1, cs, hdr)) return;
+        if (MODE == kLoadDense) finish(it, raw, v, rid, pg);
         if (pf) finish(it + 2, raw2, v2, rid2, pg2);
         if (MODE != kLoadDense) {
           cs->rowid[s][lane] = rid[0];
@@ -739,7 +741,12 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
               load_box(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y);
             }
           }
-          if (pf) prefetch_from(it + 2, v2, pg2);
+          if (pf) {
+            prefetch_from(it + 2, v2, pg2);
+          } else if (MODE == kLoadFp8 && it + 2 < ie) {
+            lookup(it + 2, v2, rid2, pg2);
+            prefetch_from(it + 2, v2, pg2);
+          }
         }
         __syncwarp();
         if (q_pending) {
@@ -784,7 +791,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kLayoutSw128);
     const uint64_t dk0 = smem_desc(smem_u32(sStage), 16, 1024, kLayoutSw128);
     int cq = 0, nseg = 0;
-    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
+    for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       nseg = si + 1;
       if (waborted(cs)) return;
       // the query's TMEM part is in place before its shared-memory part lands
@@ -867,7 +874,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     const uint32_t idesc_pv = idesc_bf16_f32(128, LC, false, true);
     const uint64_t dv0 = smem_desc(smem_u32(sStage) + (lat_x0 / 64) * C::kBox, C::kBox, 1024, kLayoutSw128);
     int cp = 0;
-    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
+    for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++cp) {
         if (waborted(cs)) return;
         const int b = cp & 1;
@@ -897,7 +904,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     // wait until every thread has read its codes.
     const int ci = tid - 192, crow = ci & 63, h = ci >> 6;
     int c = 0;
-    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
+    for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
         const int s = c % S;
@@ -973,7 +980,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     TokenPlan pend_tp{};
     int nmrg = 0;   // half partials brought in by bulk copy (buffer and phase of mrg_full / mrg_done)
     bool q_ready = false;   // the coming segment's query is already in TMEM
-    for_each_segment(a, g0, g1, t_first, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
+    for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
                                      int next_t) {
       if (waborted(cs)) return;
       if (!q_ready && !copy_q(si)) return;
