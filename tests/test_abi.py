@@ -117,3 +117,28 @@ def test_fp8_q_scale_and_sparse_mask_are_unsupported(lib):
     rc = lib.mla_decode_sparse(ctypes.byref(_dims()), ctypes.byref(_opts(mask=1)), FAKE, FAKE, 2,
                                2, FAKE, FAKE, 16, None, FAKE, FAKE, FAKE, None, FAKE, 1 << 40, None)
     assert rc == 2
+
+
+def _expected_workspace(H, L, R, T, K):
+    """The workspace sections in order, each starting on a 256-byte boundary:
+    plan header, TokenPlan[T] (32 bytes), counters int[T, 4], bounds int[2K + 1],
+    q_full bf16 [T, 128, L + R], o_lat bf16 [T, H, L], lse f32 [T, H],
+    partials f32 [K, 2, H, L] and their lse f32 [K, 2, 2, H]."""
+    up = lambda x: (x + 255) & ~255
+    o = up(256)
+    for size in (32 * max(T, 1), 16 * max(T, 1), 4 * (2 * K + 1), T * 128 * (L + R) * 2,
+                 T * H * L * 2, T * H * 4, K * 2 * H * L * 4, K * 2 * 2 * H * 4):
+        o = up(o + size)
+    return o
+
+
+@pytest.mark.parametrize("H,L,R,T,K", [(128, 512, 64, 64, 76), (128, 512, 64, 1, 1),
+                                       (16, 512, 64, 300, 37), (4, 64, 16, 5, 200)])
+def test_workspace_size_matches_the_section_layout(lib, H, L, R, T, K):
+    # the GPU plan test reads the plan, counters and bounds at these offsets
+    n = ctypes.c_size_t()
+    dims = _dims(num_heads=H, kv_lora_rank=L, qk_rope=R, qk_nope=128 if L == 512 else 32,
+                 v_head=128 if L == 512 else 32, page_size=64 if L == 512 else 16)
+    assert lib.mla_decode_workspace_size(ctypes.byref(dims), ctypes.byref(_opts(num_splits=K)), max(T, 1), T,
+                                         ctypes.byref(n)) == 0
+    assert n.value == _expected_workspace(H, L, R, T, K)
