@@ -90,8 +90,9 @@ def test_dsv3_shapes_ragged(dev, num_splits):
     check(dsv3_small(), dev, num_splits=num_splits)
 
 
-def test_null_mask(dev):
-    check(dsv3_small(mask=W.MASK_NULL, lens=(5, 130, 700)), dev)
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_null_mask(dev, num_splits):
+    check(dsv3_small(mask=W.MASK_NULL, lens=(5, 130, 700)), dev, num_splits=num_splits)
 
 
 @pytest.mark.parametrize("window", [1, 64, 100, 4096])
@@ -100,17 +101,25 @@ def test_sliding_window(dev, window):
           dev)
 
 
-def test_multi_token_queries(dev):
-    check(dsv3_small(lens=(3, 70, 300), qlens=(1, 2, 3)), dev)
+def test_sliding_window_split(dev):
+    # a few partitions: the cost-balanced plan cuts the windows into split tokens
+    check(dsv3_small(mask=W.MASK_SLIDING_WINDOW_CAUSAL, window=700, lens=(50, 300, 1000, 129)),
+          dev, num_splits=3)
+
+
+@pytest.mark.parametrize("num_splits", [0, 2, 5])
+def test_multi_token_queries(dev, num_splits):
+    check(dsv3_small(lens=(3, 70, 300), qlens=(1, 2, 3)), dev, num_splits=num_splits)
 
 
 def test_small_page_size(dev):
     check(dsv3_small(ps=16, lens=(17, 40, 333), num_pages=64), dev)
 
 
-def test_fp8_small(dev):
+@pytest.mark.parametrize("num_splits", [0, 4])
+def test_fp8_small(dev, num_splits):
     check(dsv3_small(name="fp8_small", kv_fmt="fp8", w_fmt="fp8", rms_norm=False,
-                     lens=(5, 64, 300, 900)), dev)
+                     lens=(5, 64, 300, 900)), dev, num_splits=num_splits)
 
 
 @pytest.mark.parametrize("num_splits", [0, 1, 5])
