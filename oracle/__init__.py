@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for MLA paged decode (test infrastructure).
+"""fp64 CPU oracle for MLA paged decode and for the FP8 indexer that produces the
+sparse decode's row indices (test infrastructure).
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
 may import this package.  The CUDA library never loads it, and it loads nothing
@@ -57,6 +58,19 @@ class _Args(ctypes.Structure):
     ]
 
 
+class _IndexerArgs(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int32), ("D", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("B", ctypes.c_int32), ("T", ctypes.c_int32),
+        ("mask", ctypes.c_int32), ("window", ctypes.c_int32), ("top_k", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("q_s", ctypes.c_void_p), ("row_offsets", ctypes.c_void_p),
+        ("k", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int32),
+        ("cache_lens", ctypes.c_void_p),
+        ("t_begin", ctypes.c_int32), ("t_end", ctypes.c_int32),
+    ]
+
+
 def _load():
     global _lib
     with _lock:
@@ -69,6 +83,8 @@ def _load():
             lib.mla_oracle_bf16_value.argtypes = [ctypes.c_uint16]
             lib.mla_oracle_bf16_value.restype = ctypes.c_double
             lib.mla_oracle_num_threads.restype = ctypes.c_int
+            lib.mla_oracle_indexer.argtypes = [ctypes.POINTER(_IndexerArgs), ctypes.c_void_p, ctypes.c_void_p]
+            lib.mla_oracle_indexer.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -152,3 +168,39 @@ def decode(problem, t_begin: int = 0, t_end=None):
         block_table=bt, cache_lens=p.cache_lens, indices=ind, topk_lengths=p.topk_lengths,
         w_uk=p.w_uk, w_uv=p.w_uv, w_uk_scale=p.w_uk_scale, w_uv_scale=p.w_uv_scale,
         kv_fp8=p.kv_fmt == "fp8", w_fp8=p.w_fmt == "fp8", t_begin=t_begin, t_end=t_end)
+
+
+def indexer_raw(*, H, D, page_size, mask, window, top_k, q, q_s, row_offsets, k, k_scales,
+                block_table, cache_lens, t_begin=0, t_end=None):
+    """FP8 indexer on explicit arrays (``mla_oracle_indexer`` in mla_oracle.c).  Returns
+    (rows [T, top_k] int32, scores [T, top_k] f64); rows outside [t_begin, t_end) are -2."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    q_s = np.ascontiguousarray(q_s, dtype=np.float32)
+    row_offsets = np.ascontiguousarray(row_offsets, dtype=np.uint32)
+    k = np.ascontiguousarray(k, dtype=np.uint8)
+    k_scales = np.ascontiguousarray(k_scales, dtype=np.float32)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    cache_lens = np.ascontiguousarray(cache_lens, dtype=np.uint32)
+    T, B = q.shape[0], len(row_offsets) - 1
+    if t_end is None:
+        t_end = T
+    args = _IndexerArgs(H=H, D=D, page_size=page_size, B=B, T=T, mask=mask, window=window,
+                        top_k=top_k, q=_ptr(q), q_s=_ptr(q_s), row_offsets=_ptr(row_offsets),
+                        k=_ptr(k), k_scales=_ptr(k_scales), block_table=_ptr(block_table),
+                        block_table_stride=block_table.shape[1], cache_lens=_ptr(cache_lens),
+                        t_begin=t_begin, t_end=t_end)
+    rows = np.full((T, top_k), -2, dtype=np.int32)
+    scores = np.full((T, top_k), np.nan)
+    rc = lib.mla_oracle_indexer(ctypes.byref(args), rows.ctypes.data, scores.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"mla_oracle_indexer failed with code {rc}")
+    return rows, scores
+
+
+def indexer(p, t_begin=0, t_end=None):
+    """The FP8 indexer on an :class:`workloads.indexer.IndexerProblem`."""
+    return indexer_raw(H=p.H, D=p.D, page_size=p.ps, mask=p.mask, window=p.window, top_k=p.top_k,
+                       q=p.q, q_s=p.q_s, row_offsets=p.row_offsets, k=p.k, k_scales=p.k_scales,
+                       block_table=p.block_table, cache_lens=p.cache_lens, t_begin=t_begin,
+                       t_end=t_end)

@@ -242,6 +242,104 @@ int mla_oracle_decode(const mla_oracle_args* a, double* out, double* lse) {
   return failed ? 2 : 0;
 }
 
+/*
+ * FP8 indexer, following the "mla_indexer_ragged_float8_paged" page: an FP8
+ * product of the query with the cached keys, with the query's per-head scale
+ * q_s and the key rows' scales (one per cached row, head-size granularity),
+ * summed over the heads, masked, and the top_k keys returned per query token.
+ *
+ *   score_j = sum_h q_s[t,h] * k_scale[row_j] * sum_d q[t,h,d] * k[row_j,d]
+ *
+ * Readings where the page is silent:
+ *   - the score is exactly that sum: no activation or extra weight per head;
+ *   - the key set of query token t is the decode's (causal / null /
+ *     sliding_window_causal over the request's cache_len, positions mapped to
+ *     physical rows through the block table), and the returned indices are
+ *     those physical rows, as the sparse decode consumes them;
+ *   - the rows come in descending score, equal scores in ascending key
+ *     position (so the choice does not depend on page placement), then -1
+ *     for every slot past the number of keys; a NaN score sorts last.
+ */
+typedef struct {
+  double s;
+  int64_t j, row;
+} idx_key;
+
+static int idx_key_cmp(const void* pa, const void* pb) {
+  const idx_key* a = (const idx_key*)pa;
+  const idx_key* b = (const idx_key*)pb;
+  const int na = isnan(a->s), nb = isnan(b->s);
+  if (na != nb) return na ? 1 : -1;
+  if (!na && a->s != b->s) return a->s > b->s ? -1 : 1;
+  return a->j < b->j ? -1 : (a->j > b->j ? 1 : 0);
+}
+
+int mla_oracle_indexer(const mla_oracle_indexer_args* a, int32_t* rows, double* scores) {
+  const int H = a->H, D = a->D, K = a->top_k;
+  if (a->t_begin < 0 || a->t_end > a->T || a->t_begin > a->t_end || K < 1) return 1;
+  int64_t kmax = 1;
+  for (int b = 0; b < a->B; ++b)
+    if ((int64_t)a->cache_lens[b] > kmax) kmax = a->cache_lens[b];
+  int failed = 0;
+
+#pragma omp parallel
+  {
+    idx_key* keys = (idx_key*)malloc(sizeof(idx_key) * kmax);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)H * D);
+    const int ok = keys && qv;
+    if (!ok) {
+#pragma omp atomic write
+      failed = 1;
+    }
+    {
+#pragma omp for schedule(dynamic, 1)
+      for (int t = a->t_begin; t < a->t_end; ++t) {
+        if (!ok) continue;
+        int b = 0;
+        while (b + 1 < a->B && (int64_t)a->row_offsets[b + 1] <= t) ++b;
+        const int64_t qlen = (int64_t)a->row_offsets[b + 1] - a->row_offsets[b];
+        const int64_t len = a->cache_lens[b];
+        const int64_t pos = len - qlen + (t - (int64_t)a->row_offsets[b]);
+        int64_t lo = 0, hi = len;
+        if (a->mask == MLA_ORACLE_MASK_CAUSAL) {
+          hi = pos + 1;
+        } else if (a->mask == MLA_ORACLE_MASK_SLIDING_WINDOW_CAUSAL) {
+          hi = pos + 1;
+          lo = pos + 1 - a->window;
+          if (lo < 0) lo = 0;
+        }
+        for (int h = 0; h < H; ++h)
+          for (int d = 0; d < D; ++d)
+            qv[(size_t)h * D + d] = mla_oracle_e4m3_value(a->q[((size_t)t * H + h) * D + d]);
+        int64_t n = 0;
+        for (int64_t j = lo; j < hi; ++j) {
+          const int64_t page = a->block_table[(size_t)b * a->block_table_stride + j / a->page_size];
+          const int64_t row = page * a->page_size + j % a->page_size;
+          const uint8_t* kr = a->k + (size_t)row * D;
+          double s = 0.0;
+          for (int h = 0; h < H; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += qv[(size_t)h * D + d] * mla_oracle_e4m3_value(kr[d]);
+            s += (double)a->q_s[(size_t)t * H + h] * (double)a->k_scales[row] * dot;
+          }
+          keys[n].s = s;
+          keys[n].j = j;
+          keys[n].row = row;
+          ++n;
+        }
+        qsort(keys, (size_t)n, sizeof(idx_key), idx_key_cmp);
+        for (int i = 0; i < K; ++i) {
+          rows[(size_t)t * K + i] = i < n ? (int32_t)keys[i].row : -1;
+          if (scores) scores[(size_t)t * K + i] = i < n ? keys[i].s : -INFINITY;
+        }
+      }
+    }
+    free(keys);
+    free(qv);
+  }
+  return failed ? 2 : 0;
+}
+
 int mla_oracle_num_threads(void) {
   int n = 1;
 #pragma omp parallel

@@ -45,6 +45,31 @@ typedef struct {
 /* out: [T, H, V] doubles, lse: [T, H] doubles; only tokens [t_begin, t_end) are written.
  * Returns 0 on success. */
 int mla_oracle_decode(const mla_oracle_args* a, double* out, double* lse);
+/* FP8 indexer ("mla_indexer_ragged_float8_paged"): per query token, the top_k key
+ * rows by score = sum over heads of q_s * k_scale * (q . k), e4m3 values decoded
+ * exactly.  The argument meanings are described in mla_oracle.c. */
+typedef struct {
+  int32_t H, D;              /* indexer heads, head depth */
+  int32_t page_size;
+  int32_t B, T;              /* requests, query tokens */
+  int32_t mask, window;      /* as for the decode */
+  int32_t top_k;
+  const uint8_t* q;          /* e4m3 codes [T, H, D] */
+  const float* q_s;          /* [T, H] */
+  const uint32_t* row_offsets;   /* [B+1] */
+  const uint8_t* k;          /* e4m3 codes, cache rows [rows, D] */
+  const float* k_scales;     /* [rows] */
+  const int32_t* block_table;    /* [B, block_table_stride] page ids */
+  int32_t block_table_stride;
+  const uint32_t* cache_lens;    /* [B] */
+  int32_t t_begin, t_end;    /* query tokens to evaluate */
+} mla_oracle_indexer_args;
+
+/* rows: [T, top_k] physical rows (-1 past the number of keys); scores: [T, top_k]
+ * (-inf for -1 slots) or NULL.  Only tokens [t_begin, t_end) are written.
+ * Returns 0 on success. */
+int mla_oracle_indexer(const mla_oracle_indexer_args* a, int32_t* rows, double* scores);
+
 double mla_oracle_e4m3_value(uint8_t code);
 double mla_oracle_bf16_value(uint16_t bits);
 int mla_oracle_num_threads(void);
