@@ -28,7 +28,9 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < max(
             os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "mla_oracle.h"))):
         tmp = _SO + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+        # no fused multiply-adds: the same products and sums on every machine
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-shared", "-fPIC", "-o", tmp,
+                               _SRC, "-lm"])
         os.replace(tmp, _SO)
     return _SO
 
@@ -71,6 +73,18 @@ class _IndexerArgs(ctypes.Structure):
     ]
 
 
+class _PrologueArgs(ctypes.Structure):
+    _fields_ = [
+        ("H", ctypes.c_int32), ("N", ctypes.c_int32), ("R", ctypes.c_int32), ("L", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("B", ctypes.c_int32), ("T", ctypes.c_int32),
+        ("eps", ctypes.c_double),
+        ("row_offsets", ctypes.c_void_p), ("cache_lens", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int32),
+        ("freqs_cis", ctypes.c_void_p), ("max_seq_len", ctypes.c_int32),
+        ("gamma", ctypes.c_void_p),
+    ]
+
+
 def _load():
     global _lib
     with _lock:
@@ -85,6 +99,10 @@ def _load():
             lib.mla_oracle_num_threads.restype = ctypes.c_int
             lib.mla_oracle_indexer.argtypes = [ctypes.POINTER(_IndexerArgs), ctypes.c_void_p, ctypes.c_void_p]
             lib.mla_oracle_indexer.restype = ctypes.c_int
+            lib.mla_oracle_prologue.argtypes = [ctypes.POINTER(_PrologueArgs), ctypes.c_void_p, ctypes.c_void_p]
+            lib.mla_oracle_prologue.restype = ctypes.c_int
+            lib.mla_oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.mla_oracle_round_bf16.restype = ctypes.c_uint16
             _lib = lib
     return _lib
 
@@ -204,3 +222,30 @@ def indexer(p, t_begin=0, t_end=None):
                        q=p.q, q_s=p.q_s, row_offsets=p.row_offsets, k=p.k, k_scales=p.k_scales,
                        block_table=p.block_table, cache_lens=p.cache_lens, t_begin=t_begin,
                        t_end=t_end)
+
+
+def round_bf16(x: float) -> int:
+    """fp64 -> bf16 bits, one rounding to nearest even (the oracle's own rounding)."""
+    return _load().mla_oracle_round_bf16(float(x))
+
+
+def prologue_raw(*, H, N, R, L, page_size, row_offsets, cache_lens, block_table, freqs_cis, gamma,
+                 eps, q, pool):
+    """Fused branch prologue (``mla_oracle_prologue``): returns new copies of q (bf16 bits
+    [T, H, N+R]) and pool (bf16 bits [rows, L+R]) with RoPE and RMSNorm applied."""
+    lib = _load()
+    q = np.array(q, dtype=np.uint16, copy=True, order="C")
+    pool = np.array(pool, dtype=np.uint16, copy=True, order="C")
+    row_offsets = np.ascontiguousarray(row_offsets, dtype=np.uint32)
+    cache_lens = np.ascontiguousarray(cache_lens, dtype=np.uint32)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    freqs_cis = np.ascontiguousarray(freqs_cis, dtype=np.uint16)
+    gamma = np.ascontiguousarray(gamma, dtype=np.uint16)
+    args = _PrologueArgs(H=H, N=N, R=R, L=L, page_size=page_size, B=len(row_offsets) - 1, T=q.shape[0],
+                         eps=float(eps), row_offsets=_ptr(row_offsets), cache_lens=_ptr(cache_lens),
+                         block_table=_ptr(block_table), block_table_stride=block_table.shape[1],
+                         freqs_cis=_ptr(freqs_cis), max_seq_len=freqs_cis.shape[0], gamma=_ptr(gamma))
+    rc = lib.mla_oracle_prologue(ctypes.byref(args), q.ctypes.data, pool.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"mla_oracle_prologue failed with code {rc}")
+    return q, pool

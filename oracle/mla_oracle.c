@@ -340,6 +340,97 @@ int mla_oracle_indexer(const mla_oracle_indexer_args* a, int32_t* rows, double* 
   return failed ? 2 : 0;
 }
 
+/*
+ * Fused branch prologue, following the "mla_decode_branch_fp8" page: RoPE is
+ * applied to the query and to the key cache in place, RMSNorm (kv_norm_gamma,
+ * epsilon) to the non-rope part of the key cache in place, before the absorb.
+ *
+ * Readings where the page is silent:
+ *   - freqs_cis [max_seq_len, R] holds, per position, R/2 rotations as
+ *     interleaved (cos, sin) pairs, and the rope values pair up the same way:
+ *     (x[2i], x[2i+1]) -> (x0 cos - x1 sin, x0 sin + x1 cos);
+ *   - query token t of its request sits at pos = cache_len - qlen + i (as for
+ *     the decode); its rope part turns by freqs_cis[pos], and so does the rope
+ *     part of the cache row at position pos of its request, the row this step
+ *     wrote; no other cache row changes;
+ *   - RMSNorm: c / sqrt(mean(c^2) + eps) * gamma over the L latent values;
+ *   - every result is computed in fp64 from the bf16 inputs and rounded once
+ *     to bf16 (nearest, ties to even).
+ */
+
+/* fp64 -> bf16 bits, rounded once to nearest with ties to even (finite, normal
+ * or subnormal in the bf16 range; the values here are O(1)). */
+uint16_t mla_oracle_round_bf16(double x) {
+  if (isnan(x)) return 0x7FC0;
+  const int neg = signbit(x) != 0;
+  double ax = fabs(x);
+  uint16_t out;
+  if (ax == 0.0) {
+    out = 0;
+  } else {
+    int e;
+    frexp(ax, &e);                      /* ax = m * 2^e, m in [0.5, 1) */
+    if (e < -125) e = -125;             /* bf16 subnormals: fixed quantum 2^-133 */
+    const double quantum = ldexp(1.0, e - 8);    /* 8 significant bits */
+    const double k = nearbyint(ax / quantum);    /* current mode: nearest, ties to even */
+    const double v = k * quantum;
+    if (v >= ldexp(1.0, 128)) {
+      out = 0x7F80;                     /* overflow to infinity */
+    } else {
+      const float f = (float)v;         /* exact: v has at most 8 significant bits */
+      uint32_t u;
+      memcpy(&u, &f, sizeof u);
+      out = (uint16_t)(u >> 16);
+    }
+  }
+  return (uint16_t)(out | (neg ? 0x8000 : 0));
+}
+
+int mla_oracle_prologue(const mla_oracle_prologue_args* a, uint16_t* q, uint16_t* pool) {
+  const int H = a->H, N = a->N, R = a->R, L = a->L;
+  if (R % 2 != 0) return 1;
+  int bad = 0;
+  for (int t = 0; t < a->T; ++t) {
+    int b = 0;
+    while (b + 1 < a->B && (int64_t)a->row_offsets[b + 1] <= t) ++b;
+    const int64_t qlen = (int64_t)a->row_offsets[b + 1] - a->row_offsets[b];
+    const int64_t pos = (int64_t)a->cache_lens[b] - qlen + (t - (int64_t)a->row_offsets[b]);
+    if (pos < 0 || pos >= a->max_seq_len) {
+      bad = 1;
+      continue;
+    }
+    const uint16_t* f = a->freqs_cis + (size_t)pos * R;
+    /* the query's rope part, every head */
+    for (int h = 0; h < H; ++h) {
+      uint16_t* x = q + ((size_t)t * H + h) * (size_t)(N + R) + N;
+      for (int i = 0; i < R; i += 2) {
+        const double x0 = bf16_value(x[i]), x1 = bf16_value(x[i + 1]);
+        const double c = bf16_value(f[i]), s = bf16_value(f[i + 1]);
+        x[i] = mla_oracle_round_bf16(x0 * c - x1 * s);
+        x[i + 1] = mla_oracle_round_bf16(x0 * s + x1 * c);
+      }
+    }
+    /* the cache row this token wrote */
+    const int64_t page = a->block_table[(size_t)b * a->block_table_stride + pos / a->page_size];
+    uint16_t* row = pool + (size_t)(page * a->page_size + pos % a->page_size) * (size_t)(L + R);
+    double ms = 0.0;
+    for (int l = 0; l < L; ++l) {
+      const double v = bf16_value(row[l]);
+      ms += v * v;
+    }
+    const double inv = 1.0 / sqrt(ms / L + a->eps);
+    for (int l = 0; l < L; ++l) row[l] = mla_oracle_round_bf16(bf16_value(row[l]) * inv * bf16_value(a->gamma[l]));
+    uint16_t* kr = row + L;
+    for (int i = 0; i < R; i += 2) {
+      const double x0 = bf16_value(kr[i]), x1 = bf16_value(kr[i + 1]);
+      const double c = bf16_value(f[i]), s = bf16_value(f[i + 1]);
+      kr[i] = mla_oracle_round_bf16(x0 * c - x1 * s);
+      kr[i + 1] = mla_oracle_round_bf16(x0 * s + x1 * c);
+    }
+  }
+  return bad;
+}
+
 int mla_oracle_num_threads(void) {
   int n = 1;
 #pragma omp parallel

@@ -70,6 +70,29 @@ typedef struct {
  * Returns 0 on success. */
 int mla_oracle_indexer(const mla_oracle_indexer_args* a, int32_t* rows, double* scores);
 
+/* Fused branch prologue ("mla_decode_branch_fp8"): RoPE on the query's rope part and on
+ * the rope part of each query token's own cache row, RMSNorm (gamma, eps) of that row's
+ * latent part, in place on bf16 data.  The argument meanings are described in
+ * mla_oracle.c. */
+typedef struct {
+  int32_t H, N, R, L;        /* heads, qk_nope, qk_rope (even), kv_lora_rank */
+  int32_t page_size;
+  int32_t B, T;
+  double eps;
+  const uint32_t* row_offsets;   /* [B+1] */
+  const uint32_t* cache_lens;    /* [B] */
+  const int32_t* block_table;    /* [B, block_table_stride] */
+  int32_t block_table_stride;
+  const uint16_t* freqs_cis;     /* bf16 [max_seq_len, R]: (cos, sin) per rotated pair */
+  int32_t max_seq_len;
+  const uint16_t* gamma;         /* bf16 [L] */
+} mla_oracle_prologue_args;
+
+/* q: bf16 [T, H, N+R] and pool: bf16 rows [rows, L+R], both updated in place.
+ * Returns 0 on success, 1 if a position is past max_seq_len or R is odd. */
+int mla_oracle_prologue(const mla_oracle_prologue_args* a, uint16_t* q, uint16_t* pool);
+uint16_t mla_oracle_round_bf16(double x);
+
 double mla_oracle_e4m3_value(uint8_t code);
 double mla_oracle_bf16_value(uint16_t bits);
 int mla_oracle_num_threads(void);

@@ -126,6 +126,16 @@ def to_e4m3_bits(x: np.ndarray) -> np.ndarray:
     return code | sign
 
 
+def rope_freqs_cis(max_seq_len: int, R: int, base: float = 10000.0) -> np.ndarray:
+    """bf16 bits [max_seq_len, R]: per position p and pair i, (cos, sin) of
+    p * base^(-2i/R) (a caller-side input of the fused branch prologue)."""
+    i = np.arange(R // 2, dtype=np.float64)
+    ang = np.arange(max_seq_len, dtype=np.float64)[:, None] * base ** (-2.0 * i / R)[None, :]
+    out = np.empty((max_seq_len, R), dtype=np.float64)
+    out[:, 0::2], out[:, 1::2] = np.cos(ang), np.sin(ang)
+    return to_bf16_bits(out)
+
+
 def quantise_rows_e4m3(x: np.ndarray):
     """Per-row scale = amax / 448 (float32); codes = e4m3(x / scale)."""
     amax = np.max(np.abs(x), axis=-1)
