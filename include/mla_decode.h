@@ -94,7 +94,10 @@ typedef struct {
   int32_t mask;          /* mla_mask_t */
   int32_t window;        /* tokens, >= 1 for SLIDING_WINDOW_CAUSAL, ignored otherwise */
   float scale;           /* multiplies q.k, usually 1/sqrt(N + R) */
-  int32_t num_splits;    /* KV partitions; 0 = one per pair of SMs */
+  int32_t num_splits;    /* KV partitions; 0 = one per pair of SMs.  The call cuts the
+                            batch's key tiles into that many partitions of about equal
+                            cost (tiles plus a charge per query token started); a token
+                            cut between partitions is merged in the decode kernel. */
   uint32_t flags;        /* MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_KERNEL_TIMING */
 } mla_opts_t;
 
