@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Benchmark of MLA paged decode on one GB300 (or N independent replicas).
+"""Benchmark of MLA paged decode on one GB300.
 
 One step = one full layer call of the library (plan -> W_uk absorb -> split-KV
 decode -> combine + W_uv) on the DeepSeek-V3-shaped bf16 workload: batch 64,
@@ -14,8 +14,12 @@ a sample of the workload, and an end-to-end figure through host buffers ride
 along.
 
 --impl reference times the fp64 CPU oracle (test infrastructure, never tuned)
-on bounded samples of the same workload.  Multi-GPU runs are independent
-replicas: the path needs no exchange between GPUs.
+on the same workload, one whole layer call per step.
+
+Only one GPU is used.  The decode kernel multicasts cache tiles between the two
+CTAs of a cluster, and that code is kept to single-GPU processes: with
+--gpus > 1 (or WORLD_SIZE > 1) the GPU arm prints a refusal line and exits
+without touching a device.
 """
 from __future__ import annotations
 
@@ -36,8 +40,8 @@ METRIC = "MLA decode µs/layer, HBM GB/s and tensor TFLOP/s vs roofline (B=64,H=
 UNIT = "us/layer"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 LAUNCHES_PER_CALL = 3       # absorb (+ plan), decode (+ split merge), W_uv
-CPU_SAMPLE_TOKENS = 48      # oracle sample for the CPU baseline (a few seconds of wall time)
-REF_SAMPLE_TOKENS = 2       # oracle sample per step of the reference arm
+CPU_REPEATS = 3             # oracle runs of the whole call for the CPU baseline (median)
+SINGLE_THREAD_LIMIT_S = 10  # a 1-thread oracle run longer than this is not repeated
 KERNEL_SOURCES = {"decode_splitkv": "mla_decode_attention_06_gb300/csrc/mla_decode_tc.cu"}
 
 
@@ -177,101 +181,149 @@ class ClockSampler:
                 "samples": n}
 
 
-def max_over_ranks(x: float, device=None) -> float:
-    """The slowest rank's value (every rank calls this; identity when not distributed)."""
-    import torch
-    import torch.distributed as dist
-    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
-        return x
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+def world_size():
+    return int(os.environ.get("WORLD_SIZE", "1"))
 
 
-def dist_setup(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+def rank():
+    return int(os.environ.get("RANK", "0"))
 
 
-def cpu_baseline(p, n_tokens, heads=None, seed_name="cpu-sample"):
-    """Times the oracle on a sample of query tokens (all heads, or the first `heads`)
-    and scales to one full layer call."""
-    import numpy as np
+def config_of(p, args):
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": workload_desc(p), "global_batch": p.B, "query_tokens": p.T,
+            "parallelism": "single GPU",
+            "l2": "GPU arm: a 2 x L2-size buffer is written before every timed step",
+            "num_splits": args.num_splits or "auto"}
+
+
+def oracle_call_seconds(p):
+    """Wall time of one whole layer call of the oracle (all query tokens, all heads)."""
     import oracle
-    from workloads import mla as W
     oracle.build()
-    st = W.Stream(11, seed_name)
-    toks = sorted(set(int(x) for x in st.integers(0, p.T - 1, n_tokens)))
-    pp = p
-    if heads is not None and heads < p.H:
-        import dataclasses
-        pp = dataclasses.replace(p, H=heads, q=np.ascontiguousarray(p.q[:, :heads]),
-                                 w_uk=np.ascontiguousarray(p.w_uk[:heads]),
-                                 w_uv=np.ascontiguousarray(p.w_uv[:heads]),
-                                 w_uk_scale=None if p.w_uk_scale is None else np.ascontiguousarray(p.w_uk_scale[:heads]),
-                                 w_uv_scale=None if p.w_uv_scale is None else np.ascontiguousarray(p.w_uv_scale[:heads]))
-    keys = key_counts(p)
     t0 = time.perf_counter()
-    for t in toks:
-        oracle.decode(pp, t, t + 1)
-    dt = time.perf_counter() - t0
-    # scale by attended keys: the oracle's work per token is proportional to them
-    frac = (keys[toks].sum() / keys.sum()) * (pp.H / p.H)
-    return dt / frac * 1e6, toks, oracle.num_threads(), dt
+    oracle.decode(p)
+    return time.perf_counter() - t0
+
+
+def single_thread_run(workload, repeats):
+    """The oracle on one core (a child process with OMP_NUM_THREADS=1): wall seconds of
+    `repeats` whole layer calls, each timed separately.  Stops repeating once one run
+    takes longer than SINGLE_THREAD_LIMIT_S."""
+    code = ("import json, sys, time; sys.path.insert(0, %r); import bench, oracle; "
+            "from workloads import mla as W; "
+            "p = W.config_tiny() if %r == 'tiny' else bench.make_workload(%r); "
+            "ts = []\n"
+            "for i in range(%d):\n"
+            "    ts.append(bench.oracle_call_seconds(p))\n"
+            "    if ts[-1] > %d: break\n"
+            "print(json.dumps({'seconds': ts, 'threads': oracle.num_threads()}))"
+            % (ROOT, workload, workload, repeats, SINGLE_THREAD_LIMIT_S))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout)[-300:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"us_per_call": statistics.median(d["seconds"]) * 1e6, "runs": len(d["seconds"]),
+            "threads": d["threads"]}
+
+
+def cpu_baseline(p):
+    """The oracle as it stands on the host cores: whole layer calls, median of CPU_REPEATS
+    on all cores, plus 1-thread runs of the tiny workload and of this one."""
+    import oracle
+    oracle.build()
+    secs = [oracle_call_seconds(p) for _ in range(CPU_REPEATS)]
+    us = statistics.median(secs) * 1e6
+    return {"value": us, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the whole layer call ({p.T} query tokens x {p.H} heads), "
+                      f"median of {CPU_REPEATS} runs: " + ", ".join(f"{s:.2f} s" for s in secs),
+            "single_thread": {"tiny": single_thread_run("tiny", CPU_REPEATS),
+                              p.name: single_thread_run(WORKLOAD_OF.get(p.name, "dsv3"), CPU_REPEATS)},
+            "cpu_model": cpu_model()}
+
+
+WORKLOAD_OF = {"dsv3_bf16": "dsv3", "long": "long", "long_swc": "long_swc", "fp8": "fp8",
+               "sparse": "sparse"}
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 def run_reference(args, p):
-    world, rank, local = dist_setup(args)
-    if rank != 0:
+    """The oracle timed as the reference arm: one whole layer call per step."""
+    if rank() != 0:
         return
-    times = []
-    cores = None
+    import oracle
+    oracle.build()
+    secs = []
+    w0 = time.perf_counter()
     for i in range(args.warmup + args.steps):
-        us, toks, cores, _ = cpu_baseline(p, REF_SAMPLE_TOKENS, seed_name=f"ref-step-{i}")
+        s = oracle_call_seconds(p)
         if i >= args.warmup:
-            times.append(us)
-    value = statistics.mean(times)
+            secs.append(s)
+    wall = time.perf_counter() - w0
+    ms = statistics.mean(secs) * 1e3
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3,
+        "impl": "reference", "metric": METRIC, "value": ms * 1e3, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)",
-        "config": {"workload": workload_desc(p), "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"per step: {REF_SAMPLE_TOKENS} query tokens x all heads, "
-                                   "scaled by attended keys to one layer call"},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "data": "synthetic (seeded)", "config": config_of(p, args),
+        "cpu_baseline": {"value": ms * 1e3, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step is the whole layer call ({p.T} query tokens x "
+                                   f"{p.H} heads); no scaling"},
+        "e2e": {"value": ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s_all_steps": wall,
     }
     print(json.dumps(line), flush=True)
 
 
+def refuse_multi_gpu(args):
+    """The GPU arm runs on one GPU only; under torchrun rank 0 says so and every rank exits."""
+    n = max(args.gpus, world_size())
+    if rank() == 0:
+        print(json.dumps({"impl": "ours", "metric": METRIC, "unit": UNIT, "n_gpus": n,
+                          "unavailable": "single GPU only: the decode kernel multicasts cache tiles "
+                                         "within a CTA pair, and that code runs in 1-GPU processes "
+                                         "only; the path needs no exchange between GPUs"}),
+              flush=True)
+
+
 def main():
     args = parse_args()
-    world, rank, local = dist_setup(args)
-    import numpy as np
+    p_name = args.workload
+    if args.impl == "ours" and (args.gpus > 1 or world_size() > 1):
+        refuse_multi_gpu(args)
+        return
+    if args.impl == "reference" and rank() != 0:
+        return
+    import numpy as np  # noqa: F401
     import torch
 
-    p = make_workload(args.workload, args.profile_case)
+    p = make_workload(p_name, args.profile_case)
     if args.impl == "reference":
         run_reference(args, p)
         return
 
-    import torch.distributed as dist
-    if world > 1:
-        dist.init_process_group("nccl", init_method="env://")
-    dev = torch.device(f"cuda:{local}")
+    dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
 
     from mla_decode_attention_06_gb300 import build as libbuild
     libbuild.build()
     import mla_decode_attention_06_gb300 as M
-    from workloads.run import device_inputs, run_gpu
+    from workloads.run import device_inputs, run_gpu, workspace_bytes
 
     d = device_inputs(p, dev)
-    ws = torch.empty(max(256, __import__("workloads.run", fromlist=["x"]).workspace_bytes(p, args.num_splits)),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(256, workspace_bytes(p, args.num_splits)), dtype=torch.uint8, device=dev)
     out = torch.empty((p.T, p.H, p.V), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((p.T, p.H), dtype=torch.float32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -290,10 +342,8 @@ def main():
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(0)
     time.sleep(0.25)
     w0 = time.perf_counter()
     for i in range(args.steps):
@@ -303,11 +353,9 @@ def main():
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - w0
-    if world > 1:
-        dist.barrier()
     clk = clocks.stop()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = max_over_ranks(statistics.mean(per_step), dev)
+    ms = statistics.mean(per_step)
     # per-kernel durations from separate steps: the library's event pairs between
     # its kernels would otherwise hold back the programmatic-launch overlap of the
     # timed calls above
@@ -328,19 +376,15 @@ def main():
     roof_us = max(alg["total_bytes"] / (hbm_peak * 1e9), alg["flops"] / (bf16_peak * 1e12)) * 1e6
     dec_ms = kt.get("decode_splitkv")
     dec_gbs = alg["decode_bytes"] / (dec_ms * 1e-3) / 1e9 if dec_ms else None
+    dec_tflops = alg["flops_attn"] / (dec_ms * 1e-3) / 1e12 if dec_ms else None
     traffic = kernel_traffic("decode_splitkv")
 
     line = {
-        # replicas: every rank makes one layer call per step, so the job's time per
-        # layer call is the slowest rank's step time divided by the number of ranks
-        "metric": METRIC, "value": us / world, "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if p.kv_fmt == "bf16" else "e4m3->bf16", "data": "synthetic (seeded)",
-        "config": {"workload": workload_desc(p), "global_batch": p.B * world,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)",
-                   "num_splits": args.num_splits or "auto"},
+        "config": config_of(p, args),
         "hbm_gbs": call_gbs, "tflops": call_tflops,
         "roofline_call": {"bound": "hbm" if alg["total_bytes"] / hbm_peak >= alg["flops"] / (bf16_peak * 1e3) else "tensor",
                           "roofline_us": roof_us, "frac": roof_us / us},
@@ -348,7 +392,9 @@ def main():
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": (dec_gbs / hbm_peak) if dec_gbs else None, "traffic": traffic,
                      "peak_source": f"hbm_gbs of {peak_kind}",
-                     "algorithmic_bytes_per_launch": alg["decode_bytes"]},
+                     "algorithmic_bytes_per_launch": alg["decode_bytes"],
+                     "tensor_tflops": dec_tflops,
+                     "tensor_frac": (dec_tflops / bf16_peak) if dec_tflops else None},
         "kernel_ms": {k: v for k, v in kt.items()}, "kernel_calls_timed": ncalls,
         "kernel_ms_note": "separate steps with event pairs between the kernels (no launch overlap)",
         "gpu_launches": LAUNCHES_PER_CALL * args.steps,
@@ -358,16 +404,10 @@ def main():
 
     line["graph"] = graph_replay(step, flush, stream, args.steps)
     if not args.no_e2e:
-        line["e2e"] = e2e(p, d, args, dev, out, lse, ws, flush, stream, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        us_cpu, toks, cores, dt = cpu_baseline(p, CPU_SAMPLE_TOKENS)
-        line["cpu_baseline"] = {"value": us_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{len(toks)} of {p.T} query tokens x all {p.H} heads "
-                                          f"({dt:.1f} s wall), scaled by attended keys to one call"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+        line["e2e"] = e2e(p, d, args, dev, out, lse, ws, flush, stream)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p)
+    print(json.dumps(line), flush=True)
 
 
 def graph_replay(step, flush, stream, steps):
@@ -394,7 +434,7 @@ def graph_replay(step, flush, stream, steps):
         return {"error": str(ex)[:200]}
 
 
-def e2e(p, d, args, dev, out, lse, ws, flush, stream, world):
+def e2e(p, d, args, dev, out, lse, ws, flush, stream):
     """The same call through host buffers: pinned H2D of this step's inputs (q, offsets,
     block table, cache lengths), the call, D2H of the output."""
     import torch
@@ -422,7 +462,7 @@ def e2e(p, d, args, dev, out, lse, ws, flush, stream, world):
         e.synchronize()
         if i >= 3:
             times.append(s.elapsed_time(e))
-    ms = max_over_ranks(statistics.mean(times), dev)
+    ms = statistics.mean(times)
     return {"value": ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n}
 

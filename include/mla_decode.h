@@ -180,8 +180,11 @@ int mla_decode_kernel_times(float* ms, int32_t n);
  *   - Each GPU on which this entry point's module is loaded keeps the 64 MiB
  *     until the process exits.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before capturing a stream into a CUDA graph.
+ *     (cudaGetSymbolAddress) with that device current and keeps it; make that
+ *     first call before capturing a stream into a CUDA graph.  Concurrent first
+ *     calls from several host threads are safe (the lookup is serialised).
+ *   - cudaDeviceReset invalidates the kept address: after resetting a device,
+ *     do not call this entry point on it again in the same process.
  *   - All calls share the one array: calls that may overlap on the GPU (other
  *     streams, other host threads) race and must be serialised by the caller.
  *   - Returns MLA_ERR_WORKSPACE_TOO_SMALL, with a message on stderr, when
@@ -192,6 +195,21 @@ int mla_decode_paged_static(const mla_dims_t* dims, const mla_opts_t* opts, cons
                             const void* kv_pool, const int32_t* block_table, int32_t block_table_stride,
                             const uint32_t* cache_lens, const void* w_uk, const void* w_uv, void* out,
                             float* lse_out, void* stream);
+
+/* Self-test of the failure detection (no counterpart on the API pages).  Every
+ * wait of the library's kernels is bounded in time; when one gives up, the kernel
+ * records the time-out in the workspace header and unwinds instead of hanging,
+ * and the debug path returns MLA_ERR_TIMEOUT.  This launches one thread that
+ * waits, through that same bounded wait, on a barrier nothing arrives on (no
+ * copy, MMA or other CTA involved), then reads the status back like a call with
+ * MLA_FLAG_DEBUG_CHECKS.
+ *   limit_ns    the wait's limit, 1 .. 1e9 nanoseconds
+ *   workspace   device memory, >= 256 bytes, 16-byte aligned (its header is cleared)
+ *   stream      cudaStream_t; the call synchronises it
+ * Returns MLA_ERR_TIMEOUT when the time-out was detected and reported (the
+ * expected outcome), MLA_ERR_INVALID_ARG for bad arguments, MLA_ERR_CUDA if a
+ * CUDA call failed.  The device stays usable afterwards. */
+int mla_debug_wait_selftest(uint64_t limit_ns, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Static text for a status code. */
 const char* mla_status_string(int status);

@@ -88,6 +88,25 @@ int check_opts(const mla_opts_t* o) {
   return MLA_OK;
 }
 
+// Debug path: waits for the stream, then turns the status word the kernels wrote
+// into the header into a status code (time-outs first, with where they happened).
+int device_status(const PlanHeader* hdr, cudaStream_t stream) {
+  int st_words[4] = {0, 0, 0, 0};   // status, unused, time-out record (code, block)
+  if (cudaMemcpyAsync(st_words, &hdr->status, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemcpyAsync(st_words + 2, &hdr->pad[0], 2 * sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  const int status = st_words[0];
+  if (status & kDeviceTimeout) {
+    std::fprintf(stderr, "mla_decode: device wait timed out (barrier smem offset 0x%x, thread %d, block %d)\n",
+                 st_words[2] & 0x3FFFF, (st_words[2] >> 18) & 0x1FFF, st_words[3]);
+    return MLA_ERR_TIMEOUT;
+  }
+  if (status & kDeviceCheckFailed) return MLA_ERR_DEVICE_CHECK;
+  return MLA_OK;
+}
+
 struct CallCommon {
   const mla_dims_t* d;
   const mla_opts_t* o;
@@ -189,21 +208,7 @@ int run(const CallCommon& c) {
     std::fprintf(stderr, "mla_decode: %s\n", cudaGetErrorString(e));
     return MLA_ERR_CUDA;
   }
-  if (c.o->flags & MLA_FLAG_DEBUG_CHECKS) {
-    int st_words[4] = {0, 0, 0, 0};   // status, total tiles unused, time-out record
-    if (cudaMemcpyAsync(st_words, &hdr->status, sizeof(int), cudaMemcpyDeviceToHost, c.stream) != cudaSuccess ||
-        cudaMemcpyAsync(st_words + 2, &hdr->pad[0], 2 * sizeof(int), cudaMemcpyDeviceToHost, c.stream) !=
-            cudaSuccess ||
-        cudaStreamSynchronize(c.stream) != cudaSuccess)
-      return MLA_ERR_CUDA;
-    const int status = st_words[0];
-    if (status & kDeviceTimeout) {
-      std::fprintf(stderr, "mla_decode: device wait timed out (barrier smem offset 0x%x, thread %d, block %d)\n",
-                   st_words[2] & 0x3FFFF, (st_words[2] >> 18) & 0x1FFF, st_words[3]);
-      return MLA_ERR_TIMEOUT;
-    }
-    if (status & kDeviceCheckFailed) return MLA_ERR_DEVICE_CHECK;
-  }
+  if (c.o->flags & MLA_FLAG_DEBUG_CHECKS) return device_status(hdr, c.stream);
   return MLA_OK;
 }
 
@@ -335,6 +340,20 @@ int mla_decode_kernel_times(float* ms, int32_t n) {
   }
   for (int i = 0; i < kTimedKernels && i < n; ++i) ms[i] = (float)(sum[i] / calls);
   return calls;
+}
+
+int mla_debug_wait_selftest(uint64_t limit_ns, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < sizeof(PlanHeader) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return MLA_ERR_INVALID_ARG;
+  PlanHeader* hdr = static_cast<PlanHeader*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), s) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t e = launch_wait_selftest(hdr, limit_ns, s);
+  if (e != cudaSuccess) {
+    std::fprintf(stderr, "mla_decode: %s\n", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  return device_status(hdr, s);
 }
 
 const char* mla_status_string(int status) {

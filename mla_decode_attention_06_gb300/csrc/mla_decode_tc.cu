@@ -60,7 +60,8 @@ constexpr int kMaxStages = 4;
 enum LoadMode : int {
   kLoadDense = 0,   // bf16 pool through the page table, TMA tiles multicast to the cluster
   kLoadFp8 = 1,     // e4m3 pool through the page table: TMA bytes (multicast), widened by converter warps
-  kLoadSparse = 2,  // bf16 pool rows named by an index list, TMA gather4 (each CTA its own)
+  kLoadSparse = 2,  // bf16 pool rows named by an index list, TMA gather4: each CTA gathers half
+                    // of a tile's boxes and multicasts them to both CTAs of the cluster
 };
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -1260,6 +1261,23 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   }
 }
 
+// Failure-detection self-test: one thread waits, through the same bounded wait
+// the decode uses, on an mbarrier that nothing ever arrives on.  No copy, MMA or
+// peer CTA is in flight, so giving up after `limit_ns` leaves nothing behind; the
+// time-out is recorded in the header exactly as a decode wait records it.
+__global__ void __launch_bounds__(32, 1) wait_selftest_kernel(PlanHeader* hdr, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, limit_ns)) {
+    record_timeout(&bar, hdr);
+    atomicOr(&hdr->status, kDeviceTimeout);
+  }
+}
+
 // ----------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1419,6 +1437,11 @@ bool decode_tc_supported(const mla_dims_t& d) {
   if (d.kv_lora_rank == 512 && d.qk_rope == 64) return true;
   if (d.kv_lora_rank == 64 && d.qk_rope <= 32 && d.qk_rope % 8 == 0) return true;
   return false;
+}
+
+cudaError_t launch_wait_selftest(PlanHeader* hdr, uint64_t limit_ns, cudaStream_t s) {
+  tc::wait_selftest_kernel<<<1, 32, 0, s>>>(hdr, limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s) {

@@ -40,6 +40,10 @@ cudaError_t ensure_smem_limit(const void* func, int bytes);
 bool decode_tc_supported(const mla_dims_t& d);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 
+// One thread waits (bounded by limit_ns) on an mbarrier nothing arrives on and
+// records the time-out in *hdr as a decode wait would.
+cudaError_t launch_wait_selftest(PlanHeader* hdr, uint64_t limit_ns, cudaStream_t s);
+
 // Tensor-core weight GEMMs (K1 absorb, K3 W_uv) and the split-KV combine.
 // K1: the W_uk absorb; one of its blocks also runs the plan (PlanInputs).
 struct PlanInputs;

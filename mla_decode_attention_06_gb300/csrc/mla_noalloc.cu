@@ -12,8 +12,13 @@
 // entry point has been called; with eager loading, every device).  Host code
 // must not pass the array's name to a kernel: on the host it is only a
 // stand-in symbol.  Its device address is looked up once per device with
-// cudaGetSymbolAddress, on the first call made while that device is current.
+// cudaGetSymbolAddress, on the first call made while that device is current,
+// and kept for later calls on that device.  cudaDeviceReset destroys the
+// context that address belongs to: the cached address is then stale, so a
+// process that resets a device must not call this entry point on it again.
+#include <atomic>
 #include <cstdio>
+#include <mutex>
 
 #include "mla_kernels.cuh"
 
@@ -24,22 +29,32 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-void* g_scratch_addr[kMaxDevices] = {};
+// Per device: the array's device address once looked up (published with release
+// order, so a thread that reads it non-null also sees it complete); the lookup
+// itself runs under a mutex, so concurrent first calls from several host
+// threads look it up once.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
+std::mutex g_scratch_mu;
 
 // Device address of g_static_scratch on the current device (looked up once).
 int static_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || !p) {
-      std::fprintf(stderr, "mla_decode_paged_static: cudaGetSymbolAddress failed: %s\n", cudaGetErrorString(e));
-      return MLA_ERR_CUDA;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    p = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+      if (e != cudaSuccess || !p) {
+        std::fprintf(stderr, "mla_decode_paged_static: cudaGetSymbolAddress failed: %s\n",
+                     cudaGetErrorString(e));
+        return MLA_ERR_CUDA;
+      }
+      g_scratch_addr[dev].store(p, std::memory_order_release);
     }
-    g_scratch_addr[dev] = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return MLA_OK;
 }
 

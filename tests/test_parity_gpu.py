@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from workloads import mla as W
-from workloads.run import device_inputs, run_gpu
+from workloads.run import device_inputs, run_gpu, workspace_bytes
 
 pytestmark = pytest.mark.gpu
 
@@ -57,10 +57,20 @@ def compare(p, out_gpu, lse_gpu, out_ref, lse_ref, tokens=None):
     return err.max(), rel
 
 
-def check(p, dev, num_splits=0, tokens=None):
+def split_tokens(ws, T):
+    """Query tokens the call's plan cut between KV partitions (read back from the workspace:
+    TokenPlan[T] of 8 int32 at byte 256; fields 6 and 7 are its first and last partition)."""
+    plan = ws[256:256 + 32 * T].cpu().numpy().view(np.int32).reshape(T, 8)
+    return [int(t) for t in np.flatnonzero(plan[:, 6] != plan[:, 7])]
+
+
+def check(p, dev, num_splits=0, tokens=None, with_split_tokens=True):
     d = device_inputs(p, dev)
-    out, lse = run_gpu(p, d, num_splits=num_splits, debug=True)
+    ws = torch.empty(max(256, workspace_bytes(p, num_splits)), dtype=torch.uint8, device=dev)
+    out, lse = run_gpu(p, d, num_splits=num_splits, debug=True, workspace=ws)
     torch.cuda.synchronize()
+    if tokens is not None and with_split_tokens:
+        tokens = sorted(set(tokens) | set(split_tokens(ws, p.T)))
     if tokens is None:
         ref_out, ref_lse = oracle.decode(p)
     else:
@@ -137,44 +147,74 @@ def test_sparse_without_lengths(dev):
 
 # ------------------------------------------------------------------ exactness probes
 
-def test_sparse_onehot_probe_is_bit_exact(dev):
-    """One-hot latent rows, q = 0, w_uv = identity (V = L): out * |J| must equal the exact
-    count of attended rows per latent coordinate, with -1 holes, duplicates and
-    topk_lengths honoured."""
+def _onehot_probe_problem():
+    """One-hot latent rows (row r holds e_(r mod L), rope 0), q = 0, w_uv = identity
+    (V = L): every attended row scores 0, so out * |J| is the exact multiset count of
+    attended rows per latent coordinate.  Index lists of up to 4096 slots, so that the
+    plan cuts them between partitions; at every 64-slot tile boundary a -1 hole (last
+    slot of a tile) and a duplicate (first slot of the next); topk_lengths ending on a
+    tile boundary, inside a tile, at 0 and at the full stride; valid slots past
+    topk_lengths that must be ignored; further seeded holes make each |J| a power of
+    two, so that every count / |J| is a bf16 value."""
     L = 512
-    s = W.make_sparse("probe", 41, H=128, N=128, R=64, L=L, V=L, ps=64, tokens_per_request=4096,
-                      topk_lengths=[64, 128, 32, 0, 256, 16], stride=256)
-    rows = np.zeros_like(s.rows_bf16)
+    stride = 4096
+    s = W.make_sparse("probe", 41, H=128, N=128, R=64, L=L, V=L, ps=64, tokens_per_request=8192,
+                      topk_lengths=[stride] * 5, stride=stride)
     one = W.to_bf16_bits(np.array([1.0]))[0]
-    for k, r in enumerate(s.rows_phys):
-        rows[k, int(r) % L] = one
+    rows = np.zeros_like(s.rows_bf16)
+    rows[np.arange(len(s.rows_phys)), s.rows_phys % L] = one
     ind = s.indices.copy()
-    # holes and duplicates, keeping |J| a power of two per request
-    ind[0, 0] = -1
-    ind[0, 64:65] = ind[0, 1]
-    ind[0, 3] = ind[0, 2]
-    topk = s.topk_lengths.copy()
-    topk[0] = 65
-    ind[1, 128:] = ind[1, 0]       # garbage beyond topk_lengths
+    topk = np.array([4096, 2113, 1088, 0, 70], dtype=np.int32)
+    st = W.Stream(43, "probe-holes")
+    for b in range(s.B):
+        for k in range(64, stride, 64):
+            ind[b, k - 1] = -1                  # hole: last slot of a tile
+            ind[b, k] = ind[b, k + 1]           # duplicate: first slot of the next tile
+        n = int(topk[b])
+        valid = np.flatnonzero(ind[b, :n] >= 0)
+        if len(valid):
+            target = 1 << (len(valid).bit_length() - 1)
+            drop = valid[st.permutation(len(valid))[:len(valid) - target]]
+            ind[b, drop] = -1
+        if n < stride:
+            ind[b, n:] = s.indices[b, 0]       # valid rows past topk_lengths: ignored
     eye = np.zeros((s.H, L, L), dtype=np.uint16)
     eye[:, np.arange(L), np.arange(L)] = one
-    p = dataclasses.replace(s, rows_bf16=rows, indices=ind, topk_lengths=topk,
-                            q=np.zeros_like(s.q), w_uv=eye)
+    return dataclasses.replace(s, rows_bf16=rows, indices=ind, topk_lengths=topk,
+                               q=np.zeros_like(s.q), w_uv=eye), L
+
+
+@pytest.mark.parametrize("num_splits", [1, 0, 5, 64, 200])
+def test_sparse_onehot_probe_is_bit_exact(dev, num_splits):
+    """The sparse index handling (-1 holes, duplicates, topk_lengths) is exact also where
+    the plan cuts an index list between partitions: a dropped or doubled row changes a
+    count by one.  A merge weighs each partition's count vector by
+    exp(lse_p - lse) = |J_p| / |J| in fp32; the merged value is within a few fp32 ulps
+    of count / |J|, a bf16 value, so the bf16 latent output and hence out are exact."""
+    p, L = _onehot_probe_problem()
+    ind, topk = p.indices, p.topk_lengths
     d = device_inputs(p, dev)
-    out, lse = run_gpu(p, d, num_splits=1, debug=True)
-    out = out.float().cpu().numpy()
+    ws = torch.empty(max(256, workspace_bytes(p, num_splits)), dtype=torch.uint8, device=dev)
+    out, lse = run_gpu(p, d, num_splits=num_splits, debug=True, workspace=ws)
+    torch.cuda.synchronize()
+    if num_splits != 1:
+        assert split_tokens(ws, p.T), "the plan should cut some index lists"
+    out = out.float().cpu().numpy().astype(np.float64)
     lse = lse.cpu().numpy()
     for b in range(p.B):
         J = [int(x) for x in ind[b, :int(topk[b])] if x >= 0]
         counts = np.zeros(L)
         for r in J:
             counts[r % L] += 1
-        for h in range(p.H):
-            if J:
-                assert np.array_equal(out[b, h].astype(np.float64) * len(J), counts), (b, h)
-                assert abs(lse[b, h] - math.log(len(J))) < 1e-6
-            else:
-                assert np.all(out[b, h] == 0) and np.isneginf(lse[b, h])
+        if J:
+            assert len(J) & (len(J) - 1) == 0
+            scaled = out[b] * len(J)
+            assert np.max(np.abs(scaled - counts[None, :])) < 1e-3, b
+            assert np.array_equal(np.rint(scaled), np.broadcast_to(counts, scaled.shape)), b
+            assert np.array_equal(scaled, np.broadcast_to(counts, scaled.shape)), b
+            assert np.max(np.abs(lse[b] - math.log(len(J)))) < 1e-5, b
+        else:
+            assert np.all(out[b] == 0) and np.all(np.isneginf(lse[b])), b
 
 
 def test_page_permutation_is_bit_identical(dev):
@@ -216,33 +256,54 @@ def test_bad_page_id_is_reported_not_dereferenced(dev):
 
 
 # ------------------------------------------------------------------ full-size workloads
-# sampled outputs: the oracle evaluates a few query tokens (all heads) of the full call
+# the oracle evaluates sampled query tokens (all heads) of the full call, every token the
+# plan splits between partitions among them (all tokens for long context and sparse)
 
-def _sample(p, k=3):
+def _sample(p, k):
     st = W.Stream(7, p.name + "-sample")
-    return sorted(set(int(x) for x in st.integers(0, p.T - 1, k)))
+    return sorted(set(int(x) for x in st.integers(0, p.T - 1, 4 * k)))[:k]
+
+
+def _split_invariance(p, dev):
+    """Every query token of the full call: the launch configuration timed by the benchmark
+    (auto splits) against one partition walking the whole batch.  Unsplit tokens round
+    the latent output to bf16 before W_uv, split ones merge fp32 partials first, so the
+    two differ by bf16 rounding of o only."""
+    d = device_inputs(p, dev)
+    one, _ = run_gpu(p, d, num_splits=1, debug=True)
+    auto, _ = run_gpu(p, d, num_splits=0, debug=True)
+    torch.cuda.synchronize()
+    a, b = auto.float(), one.float()
+    assert torch.isfinite(a).all()
+    assert (a - b).abs().max().item() <= 2e-2
+    assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() <= 2e-3
 
 
 def test_full_dsv3_bf16(dev):
     p = W.config_dsv3()
-    check(p, dev, tokens=_sample(p))
+    check(p, dev, tokens=_sample(p, 16))
+    _split_invariance(p, dev)
 
 
 def test_full_long_context(dev):
     p = W.config_long()
-    check(p, dev, tokens=_sample(p, 2))
+    check(p, dev, tokens=list(range(p.T)))
+    _split_invariance(p, dev)
 
 
 def test_full_long_sliding_window(dev):
     p = W.config_long(window=4096)
-    check(p, dev, tokens=_sample(p, 3))
+    check(p, dev, tokens=list(range(p.T)))
+    _split_invariance(p, dev)
 
 
 def test_full_fp8(dev):
     p = W.config_fp8()
-    check(p, dev, tokens=_sample(p, 3))
+    check(p, dev, tokens=_sample(p, 16))
+    _split_invariance(p, dev)
 
 
 def test_full_sparse(dev):
     p = W.config_sparse()
-    check(p, dev, tokens=_sample(p, 4))
+    check(p, dev)
+    _split_invariance(p, dev)
