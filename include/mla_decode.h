@@ -160,6 +160,37 @@ int mla_decode_sparse(const mla_dims_t* dims, const mla_opts_t* opts, const void
                       void* out, float* lse_out, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/* Fused branch prologue (mla_decode_branch_fp8 page, description: "Apply RoPE to
+ * the query and the key cache (in-place)", "Apply RMSNorm to the non-rope portion
+ * of the key cache (in-place)"; Args freqs_cis, kv_norm_gamma, epsilon), run
+ * before the decode call of the same step.  For query token t of request b at
+ * position pos = cache_lens[b] - qlen + i:
+ *   - q[t, h, N + 2i], q[t, h, N + 2i + 1] of every head turn by
+ *     freqs_cis[pos, 2i] = cos, freqs_cis[pos, 2i + 1] = sin:
+ *     (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos);
+ *   - the cache row at position pos of request b (the row this step wrote):
+ *     latent part c -> c / sqrt(mean(c^2) + epsilon) * kv_norm_gamma, rope part
+ *     turned like the query's;
+ *   - no other value changes.
+ * Every result is the double-precision value of those expressions (each product
+ * and sum rounded separately, the mean square summed in latent order) rounded
+ * once to bf16, nearest with ties to even.
+ *   q              bf16 [T, H, N+R], rope part rewritten in place
+ *   kv_pool        bf16 [num_pages, ps, L+R] (L <= 512), rows rewritten in place
+ *   freqs_cis      bf16 [max_seq_len, R]: per position R/2 (cos, sin) pairs
+ *   kv_norm_gamma  bf16 [L]
+ *   epsilon        >= 0
+ *   flags          0 or MLA_FLAG_DEBUG_CHECKS (wait and report device checks)
+ *   workspace      device memory, >= 256 bytes, 16-byte aligned (status word)
+ * Other arguments as mla_decode_paged.  A token whose position is outside
+ * [0, max_seq_len) or whose page id is outside [0, num_pages) is left unchanged
+ * (query and row) and recorded: MLA_ERR_DEVICE_CHECK in debug mode. */
+int mla_branch_prologue(const mla_dims_t* dims, void* q, const uint32_t* input_row_offsets, int32_t batch,
+                        int32_t total_q, void* kv_pool, const int32_t* block_table, int32_t block_table_stride,
+                        const uint32_t* cache_lens, const void* freqs_cis, int32_t max_seq_len,
+                        const void* kv_norm_gamma, float epsilon, uint32_t flags, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* Mean per-kernel device durations (milliseconds) over the calls on the current
  * device that set MLA_FLAG_KERNEL_TIMING since the previous read (at most the
  * last 4096), in launch order: [0] W_uk absorb (with the call's planning),

@@ -9,6 +9,7 @@ Entry points (same names as the C ABI):
   mla_decode_paged      bf16 paged cache
   mla_decode_paged_fp8  e4m3 latent cache with one fp32 scale per row, e4m3 weights
   mla_decode_sparse     attention restricted to given physical cache rows
+  mla_branch_prologue   RoPE on q and the new cache rows, RMSNorm of their latent part
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ from . import _lib
 from ._lib import (MLA_FLAG_DEBUG_CHECKS, MLA_FLAG_KERNEL_TIMING, MLA_MASK_CAUSAL, MLA_MASK_NULL,
                    MLA_MASK_SLIDING_WINDOW_CAUSAL, MlaDims, MlaError, MlaOpts, kernel_times)
 
-__all__ = ["mla_decode_paged", "mla_decode_paged_fp8", "mla_decode_sparse",
+__all__ = ["mla_decode_paged", "mla_decode_paged_fp8", "mla_decode_sparse", "mla_branch_prologue",
            "mla_decode_workspace_size", "MlaDims", "MlaOpts", "MlaError", "MLA_MASK_NULL",
            "MLA_MASK_CAUSAL", "MLA_MASK_SLIDING_WINDOW_CAUSAL", "library_path", "kernel_times"]
 
@@ -182,3 +183,38 @@ def mla_decode_sparse(q, input_row_offsets, kv_pool, d_indices, topk_lengths, w_
     if rc:
         raise MlaError("mla_decode_sparse", rc)
     return out, lse_out
+
+
+def mla_branch_prologue(q, input_row_offsets, kv_pool, block_table, cache_lens, freqs_cis,
+                        kv_norm_gamma, *, page_size: int, kv_lora_rank: int, epsilon: float,
+                        debug: bool = False, workspace=None, stream=None):
+    """In place: RoPE on q's rope part and, per query token, RMSNorm + RoPE of the cache
+    row at its position.  q bf16 [T,H,N+R]; kv_pool bf16 rows of L+R (L = kv_lora_rank);
+    freqs_cis bf16 [max_seq_len, R]; kv_norm_gamma bf16 [L].  Returns (q, kv_pool)."""
+    dev = q.device
+    T, H, NR = q.shape
+    B = input_row_offsets.numel() - 1
+    L = int(kv_lora_rank)
+    R = freqs_cis.shape[1]
+    row_bytes = 2 * (L + R)
+    pool_bytes = kv_pool.numel() * kv_pool.element_size()
+    if pool_bytes % (page_size * row_bytes):
+        raise ValueError("kv pool size is not a whole number of pages")
+    dims = MlaDims(num_heads=H, qk_nope=NR - R, qk_rope=R, kv_lora_rank=L, v_head=1,
+                   page_size=page_size, num_pages=pool_bytes // (page_size * row_bytes))
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=dev)
+    i32 = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+    rc = _lib.load().mla_branch_prologue(
+        ctypes.byref(dims), _ptr(q, "q", (torch.bfloat16,), dev),
+        _ptr(input_row_offsets, "input_row_offsets", i32, dev), B, T,
+        _ptr(kv_pool, "kv_pool", None, dev), _ptr(block_table, "block_table", (torch.int32,), dev),
+        block_table.shape[1], _ptr(cache_lens, "cache_lens", i32, dev),
+        _ptr(freqs_cis, "freqs_cis", (torch.bfloat16,), dev), freqs_cis.shape[0],
+        _ptr(kv_norm_gamma, "kv_norm_gamma", (torch.bfloat16,), dev), float(epsilon),
+        MLA_FLAG_DEBUG_CHECKS if debug else 0,
+        _ptr(workspace, "workspace", None, dev), workspace.numel() * workspace.element_size(),
+        _stream(stream, dev))
+    if rc:
+        raise MlaError("mla_branch_prologue", rc)
+    return q, kv_pool

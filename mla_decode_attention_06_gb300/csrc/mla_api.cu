@@ -342,6 +342,35 @@ int mla_decode_kernel_times(float* ms, int32_t n) {
   return calls;
 }
 
+int mla_branch_prologue(const mla_dims_t* dims, void* q, const uint32_t* input_row_offsets, int32_t batch,
+                        int32_t total_q, void* kv_pool, const int32_t* block_table, int32_t block_table_stride,
+                        const uint32_t* cache_lens, const void* freqs_cis, int32_t max_seq_len,
+                        const void* kv_norm_gamma, float epsilon, uint32_t flags, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!dims || dims->num_heads < 1 || dims->qk_nope < 0 || dims->qk_rope < 2 || dims->qk_rope % 2 != 0 ||
+      dims->kv_lora_rank < 1 || dims->kv_lora_rank > 512 || dims->page_size < 1 || dims->num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if ((int64_t)dims->num_pages * dims->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (batch < 1 || total_q < 0 || block_table_stride < 1 || max_seq_len < 1) return MLA_ERR_INVALID_ARG;
+  if (!q || !input_row_offsets || !kv_pool || !block_table || !cache_lens || !freqs_cis || !kv_norm_gamma ||
+      !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (!(epsilon >= 0.f) || (flags & ~MLA_FLAG_DEBUG_CHECKS)) return MLA_ERR_INVALID_ARG;
+  if (workspace_bytes < sizeof(PlanHeader) || !aligned16(workspace)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  PlanHeader* hdr = static_cast<PlanHeader*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), s) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t e = launch_prologue(*dims, q, input_row_offsets, batch, total_q, kv_pool, block_table,
+                                        block_table_stride, cache_lens, freqs_cis, max_seq_len, kv_norm_gamma,
+                                        epsilon, hdr, s);
+  if (e != cudaSuccess) {
+    std::fprintf(stderr, "mla_branch_prologue: %s\n", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  if (flags & MLA_FLAG_DEBUG_CHECKS) return device_status(hdr, s);
+  return MLA_OK;
+}
+
 int mla_debug_wait_selftest(uint64_t limit_ns, void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < sizeof(PlanHeader) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   if (limit_ns == 0 || limit_ns > 1000000000ull) return MLA_ERR_INVALID_ARG;

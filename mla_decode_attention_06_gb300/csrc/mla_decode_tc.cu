@@ -64,6 +64,9 @@ enum LoadMode : int {
                     // of a tile's boxes and multicasts them to both CTAs of the cluster
 };
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
+// The producer reads the page-table entries of the tile this many ahead of the one it
+// loads and prefetches that tile's boxes into L2.
+constexpr int kPrefetchAhead = 2;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 struct Smem {   // control block after the stage ring
@@ -73,6 +76,7 @@ struct Smem {   // control block after the stage ring
   uint64_t q_full, q_empty;
   uint64_t qa_full, qa_done;     // query latent [0, QT) staged in shared memory / moved into TMEM
   uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t pv_iss;               // the P . C of a tile has been issued (orders the next QK's second half)
   uint64_t o_free;
   uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
   uint64_t fix_bar, fix_done;    // softmax: partial written / claim outcome published
@@ -497,6 +501,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       mbar_init(&cs->p_full[b], 128);
       mbar_init(&cs->pv_done[b], 1);
     }
+    mbar_init(&cs->pv_iss, 1);
     mbar_init(&cs->o_free, 128);
     mbar_init(&cs->conv_sync, C::kConvThreads);
     mbar_init(&cs->fix_bar, 128);
@@ -664,15 +669,15 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         // tile two ahead after issuing this one's loads instead.
         int raw[2], raw2[2];
         fetch(it, raw);
-        const bool pf = MODE == kLoadDense && it + 2 < ie;
-        if (pf) fetch(it + 2, raw2);
+        const bool pf = MODE == kLoadDense && it + kPrefetchAhead < ie;
+        if (pf) fetch(it + kPrefetchAhead, raw2);
         bool v[2], v2[2];
         int rid[2], pg[2], rid2[2], pg2[2];
         if (MODE != kLoadDense) finish(it, raw, v, rid, pg);
         // stage s is free in both CTAs once both have committed their P . C of its last tile
         if (c >= S && !wwait(&cs->kv_empty[s], ((c / S) & 1) ^ 1, cs, hdr)) return;
         if (MODE == kLoadDense) finish(it, raw, v, rid, pg);
-        if (pf) finish(it + 2, raw2, v2, rid2, pg2);
+        if (pf) finish(it + kPrefetchAhead, raw2, v2, rid2, pg2);
         if (MODE != kLoadDense) {
           cs->rowid[s][lane] = rid[0];
           cs->rowid[s][lane + 32] = rid[1];
@@ -743,10 +748,10 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             }
           }
           if (pf) {
-            prefetch_from(it + 2, v2, pg2);
-          } else if (MODE == kLoadFp8 && it + 2 < ie) {
-            lookup(it + 2, v2, rid2, pg2);
-            prefetch_from(it + 2, v2, pg2);
+            prefetch_from(it + kPrefetchAhead, v2, pg2);
+          } else if (MODE == kLoadFp8 && it + kPrefetchAhead < ie) {
+            lookup(it + kPrefetchAhead, v2, rid2, pg2);
+            prefetch_from(it + kPrefetchAhead, v2, pg2);
           }
         }
         __syncwarp();
@@ -847,6 +852,14 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           tc_fence_after();
           q_smem = true;
         }
+        // The tensor pipe runs MMAs in issue order.  The previous tile's P . C
+        // frees its cache stage for the next load, so it goes ahead of this
+        // tile's second half: wait until it has been issued (its P is computed
+        // while the first half runs).
+        if (cq >= 1) {
+          __syncwarp();
+          if (!wwait(&cs->pv_iss, (cq - 1) & 1, cs, hdr)) return;
+        }
         if (lane == 0) {
 #pragma unroll 1
           for (int i = 0; i <= C::NQS; ++i) {
@@ -892,6 +905,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           if (CL == 2) mma_commit_mc(&cs->kv_empty[cp % S], (uint16_t)0x3);
           else mma_commit(&cs->kv_empty[cp % S]);
           mma_commit(&cs->pv_done[b]);
+          mbar_arrive(&cs->pv_iss);
         }
         __syncwarp();
       }

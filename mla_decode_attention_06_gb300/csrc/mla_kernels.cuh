@@ -56,4 +56,11 @@ cudaError_t launch_uv_tc(const mla_dims_t& d, int T, const __nv_bfloat16* o_lat,
 
 
 
+// The fused branch prologue: RoPE on the query's rope part and, for each query
+// token, RMSNorm + RoPE of the cache row at its position (bf16 pool), in place.
+cudaError_t launch_prologue(const mla_dims_t& d, void* q, const uint32_t* offsets, int B, int T, void* kv_pool,
+                            const int32_t* block_table, int bt_stride, const uint32_t* cache_lens,
+                            const void* freqs, int max_seq_len, const void* gamma, float eps, PlanHeader* hdr,
+                            cudaStream_t s);
+
 }  // namespace mla

@@ -266,17 +266,25 @@ def _sample(p, k):
 
 def _split_invariance(p, dev):
     """Every query token of the full call: the launch configuration timed by the benchmark
-    (auto splits) against one partition walking the whole batch.  Unsplit tokens round
-    the latent output to bf16 before W_uv, split ones merge fp32 partials first, so the
-    two differ by bf16 rounding of o only."""
+    (auto splits) against one partition walking the whole batch.  The two round
+    differently (other running maxima behind the bf16 P, partials merged in fp32), and
+    each is within the oracle tolerance of the exact result, so they must agree within
+    that tolerance overall and within twice it for every token; a partition dropped or
+    counted twice moves a token by far more."""
     d = device_inputs(p, dev)
     one, _ = run_gpu(p, d, num_splits=1, debug=True)
     auto, _ = run_gpu(p, d, num_splits=0, debug=True)
     torch.cuda.synchronize()
     a, b = auto.float(), one.float()
     assert torch.isfinite(a).all()
-    assert (a - b).abs().max().item() <= 2e-2
-    assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() <= 2e-3
+    tol = TOL_FP8_REL_L2 if p.kv_fmt == "fp8" else TOL_BF16_REL_L2
+    assert (a - b).abs().max().item() <= 2 * TOL_BF16_MAX_ABS
+    assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() <= tol
+    nb = torch.linalg.norm(b.flatten(1), dim=1)
+    live = nb > 0
+    assert torch.equal(a.flatten(1)[~live], b.flatten(1)[~live])     # tokens without keys: zeros
+    per_token = torch.linalg.norm((a - b).flatten(1)[live], dim=1) / nb[live]
+    assert per_token.max().item() <= 2 * tol, per_token.max().item()
 
 
 def test_full_dsv3_bf16(dev):
