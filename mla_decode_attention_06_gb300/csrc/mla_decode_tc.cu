@@ -76,7 +76,6 @@ struct Smem {   // control block after the stage ring
   uint64_t q_full, q_empty;
   uint64_t qa_full, qa_done;     // query latent [0, QT) staged in shared memory / moved into TMEM
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t pv_iss;               // the P . C of a tile has been issued (orders the next QK's second half)
   uint64_t o_free;
   uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
   uint64_t fix_bar, fix_done;    // softmax: partial written / claim outcome published
@@ -501,7 +500,6 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       mbar_init(&cs->p_full[b], 128);
       mbar_init(&cs->pv_done[b], 1);
     }
-    mbar_init(&cs->pv_iss, 1);
     mbar_init(&cs->o_free, 128);
     mbar_init(&cs->conv_sync, C::kConvThreads);
     mbar_init(&cs->fix_bar, 128);
@@ -852,14 +850,6 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           tc_fence_after();
           q_smem = true;
         }
-        // The tensor pipe runs MMAs in issue order.  The previous tile's P . C
-        // frees its cache stage for the next load, so it goes ahead of this
-        // tile's second half: wait until it has been issued (its P is computed
-        // while the first half runs).
-        if (cq >= 1) {
-          __syncwarp();
-          if (!wwait(&cs->pv_iss, (cq - 1) & 1, cs, hdr)) return;
-        }
         if (lane == 0) {
 #pragma unroll 1
           for (int i = 0; i <= C::NQS; ++i) {
@@ -905,7 +895,6 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           if (CL == 2) mma_commit_mc(&cs->kv_empty[cp % S], (uint16_t)0x3);
           else mma_commit(&cs->kv_empty[cp % S]);
           mma_commit(&cs->pv_done[b]);
-          mbar_arrive(&cs->pv_iss);
         }
         __syncwarp();
       }
