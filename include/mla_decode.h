@@ -191,6 +191,43 @@ int mla_branch_prologue(const mla_dims_t* dims, void* q, const uint32_t* input_r
                         const void* kv_norm_gamma, float epsilon, uint32_t flags, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* FP8 indexer (mla_indexer_ragged_float8_paged page: the FP8 product of the query
+ * with the key cache, with the query's per-head scales q_s and the key scales at
+ * head-size granularity, summed across the heads, masked, top-k; Args
+ * output_indices, -1 where fewer keys exist).  It produces the row lists
+ * mla_decode_sparse consumes.  For query token t of request b and every key j of
+ * its key set (the decode's mask rules over cache_lens[b]):
+ *   s_j = sum_h (q_s[t,h] * k_scales[row_j]) * (sum_d q[t,h,d] * k_cache[row_j,d])
+ * output_indices[t, i] for i < top_k: the physical rows (page * ps + slot) of the
+ * keys by descending s_j, equal scores by ascending position j, NaN scores last;
+ * -1 past the number of keys.  The inner sum is exact (an e4m3 value is a multiple
+ * of 2^-9, so the sum is an exact integer multiple of 2^-18) and the head sum is
+ * the double-precision value of that expression evaluated in head order, each
+ * product and sum rounded separately: the ranking, ties included, is exactly
+ * defined.
+ *   q               e4m3 (OCP E4M3FN) [T, H, D] with H = num_heads, D = head_dim
+ *   q_s             float [T, H]
+ *   k_cache         e4m3 [num_pages, ps, D]
+ *   k_scales        float [num_pages, ps]
+ *   mask, window    as mla_opts_t (NULL, CAUSAL or SLIDING_WINDOW_CAUSAL)
+ *   top_k           1 .. 4096
+ *   output_indices  int32 [T, top_k]
+ *   output_scores   double [T, top_k] (s_j of each returned row, -inf for -1 slots) or NULL
+ *   flags           0 or MLA_FLAG_DEBUG_CHECKS
+ *   workspace       mla_indexer_workspace_size() bytes, 16-byte aligned
+ * Other arguments as mla_decode_paged.  Keys on a page id outside [0, num_pages)
+ * are never read: they come out as -1 and are recorded (MLA_ERR_DEVICE_CHECK in
+ * debug mode).  Shapes whose per-block scratch exceeds the limit
+ * (2 H D + 64 D + 256 H bytes, about 200 KB) return MLA_ERR_UNSUPPORTED. */
+int mla_indexer_workspace_size(int32_t total_q, int32_t block_table_stride, int32_t page_size, int32_t mask,
+                               int32_t window, size_t* bytes);
+int mla_indexer_fp8(int32_t num_heads, int32_t head_dim, int32_t page_size, int32_t num_pages, const void* q,
+                    const float* q_s, const uint32_t* input_row_offsets, int32_t batch, int32_t total_q,
+                    const void* k_cache, const float* k_scales, const int32_t* block_table,
+                    int32_t block_table_stride, const uint32_t* cache_lens, int32_t mask, int32_t window,
+                    int32_t top_k, int32_t* output_indices, double* output_scores, uint32_t flags,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Mean per-kernel device durations (milliseconds) over the calls on the current
  * device that set MLA_FLAG_KERNEL_TIMING since the previous read (at most the
  * last 4096), in launch order: [0] W_uk absorb (with the call's planning),

@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
   mla_decode_paged_fp8  e4m3 latent cache with one fp32 scale per row, e4m3 weights
   mla_decode_sparse     attention restricted to given physical cache rows
   mla_branch_prologue   RoPE on q and the new cache rows, RMSNorm of their latent part
+  mla_indexer_fp8       top-k cache rows per query token by FP8 index scores (sparse input)
 """
 from __future__ import annotations
 
@@ -24,6 +25,7 @@ from ._lib import (MLA_FLAG_DEBUG_CHECKS, MLA_FLAG_KERNEL_TIMING, MLA_MASK_CAUSA
                    MLA_MASK_SLIDING_WINDOW_CAUSAL, MlaDims, MlaError, MlaOpts, kernel_times)
 
 __all__ = ["mla_decode_paged", "mla_decode_paged_fp8", "mla_decode_sparse", "mla_branch_prologue",
+           "mla_indexer_fp8",
            "mla_decode_workspace_size", "MlaDims", "MlaOpts", "MlaError", "MLA_MASK_NULL",
            "MLA_MASK_CAUSAL", "MLA_MASK_SLIDING_WINDOW_CAUSAL", "library_path", "kernel_times"]
 
@@ -218,3 +220,44 @@ def mla_branch_prologue(q, input_row_offsets, kv_pool, block_table, cache_lens, 
     if rc:
         raise MlaError("mla_branch_prologue", rc)
     return q, kv_pool
+
+
+def mla_indexer_fp8(q, q_s, input_row_offsets, k_cache, k_scales, block_table, cache_lens, *,
+                    page_size: int, top_k: int, mask: int = MLA_MASK_CAUSAL, window: int = 0,
+                    with_scores: bool = False, debug: bool = False, out=None, workspace=None,
+                    stream=None):
+    """Top-k physical cache rows per query token.  q e4m3 codes [T,H,D] (uint8 or
+    float8_e4m3fn), q_s f32 [T,H], k_cache e4m3 codes (page-major rows of D), k_scales f32
+    [rows].  Returns (indices int32 [T, top_k], scores f64 [T, top_k] or None)."""
+    dev = q.device
+    T, H, D = q.shape
+    B = input_row_offsets.numel() - 1
+    rows = k_cache.numel() // D
+    if rows % page_size:
+        raise ValueError("k_cache is not a whole number of pages")
+    lib = _lib.load()
+    need = ctypes.c_size_t(0)
+    rc = lib.mla_indexer_workspace_size(T, block_table.shape[1], page_size, int(mask), int(window),
+                                        ctypes.byref(need))
+    if rc:
+        raise MlaError("mla_indexer_workspace_size", rc)
+    if workspace is None:
+        workspace = torch.empty(need.value, dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty((T, top_k), dtype=torch.int32, device=dev)
+    scores = torch.empty((T, top_k), dtype=torch.float64, device=dev) if with_scores else None
+    i32 = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+    f8 = (torch.uint8, torch.float8_e4m3fn)
+    rc = lib.mla_indexer_fp8(
+        H, D, page_size, rows // page_size, _ptr(q, "q", f8, dev), _ptr(q_s, "q_s", (torch.float32,), dev),
+        _ptr(input_row_offsets, "input_row_offsets", i32, dev), B, T,
+        _ptr(k_cache, "k_cache", f8, dev), _ptr(k_scales, "k_scales", (torch.float32,), dev),
+        _ptr(block_table, "block_table", (torch.int32,), dev), block_table.shape[1],
+        _ptr(cache_lens, "cache_lens", i32, dev), int(mask), int(window), int(top_k),
+        _ptr(out, "out", (torch.int32,), dev), _ptr(scores, "scores", (torch.float64,), dev),
+        MLA_FLAG_DEBUG_CHECKS if debug else 0,
+        _ptr(workspace, "workspace", None, dev), workspace.numel() * workspace.element_size(),
+        _stream(stream, dev))
+    if rc:
+        raise MlaError("mla_indexer_fp8", rc)
+    return out, scores

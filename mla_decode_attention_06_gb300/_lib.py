@@ -27,6 +27,7 @@ KERNEL_NAMES = ("absorb_w_uk", "decode_splitkv", "w_uv")
 
 EXPORTED = ("mla_decode_workspace_size", "mla_decode_paged", "mla_decode_paged_fp8",
             "mla_decode_sparse", "mla_decode_kernel_times", "mla_branch_prologue",
+            "mla_indexer_workspace_size", "mla_indexer_fp8",
             "mla_debug_wait_selftest",
             "mla_status_string")
 
@@ -56,6 +57,10 @@ _SIGS = {
                           c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                           c_void_p, c_size_t, c_void_p],
     "mla_debug_wait_selftest": [ctypes.c_uint64, c_void_p, c_size_t, c_void_p],
+    "mla_indexer_workspace_size": [c_int32, c_int32, c_int32, c_int32, c_int32, _P(c_size_t)],
+    "mla_indexer_fp8": [c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int32,
+                        c_int32, c_void_p, c_void_p, c_void_p, c_int32, c_void_p, c_int32, c_int32,
+                        c_int32, c_void_p, c_void_p, c_uint32, c_void_p, c_size_t, c_void_p],
     "mla_branch_prologue": [_P(MlaDims), c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p,
                             c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_float, c_uint32,
                             c_void_p, c_size_t, c_void_p],

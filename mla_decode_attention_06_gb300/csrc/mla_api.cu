@@ -371,6 +371,67 @@ int mla_branch_prologue(const mla_dims_t* dims, void* q, const uint32_t* input_r
   return MLA_OK;
 }
 
+namespace {
+constexpr int kIndexerMaxTopK = 4096;
+constexpr size_t kIndexerMaxScoreSmem = 200 * 1024;
+
+int indexer_max_keys(int32_t stride, int32_t ps, int32_t mask, int32_t window) {
+  const int64_t cap = (int64_t)stride * ps;
+  if (mask == MLA_MASK_SLIDING_WINDOW_CAUSAL && window < cap) return window;
+  return (int)cap;
+}
+}  // namespace
+
+int mla_indexer_workspace_size(int32_t total_q, int32_t block_table_stride, int32_t page_size, int32_t mask,
+                               int32_t window, size_t* bytes) {
+  if (!bytes || total_q < 0 || block_table_stride < 1 || page_size < 1) return MLA_ERR_INVALID_ARG;
+  if ((int64_t)block_table_stride * page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (mask == MLA_MASK_SLIDING_WINDOW_CAUSAL && window < 1) return MLA_ERR_INVALID_ARG;
+  *bytes = indexer_workspace_bytes(total_q, indexer_max_keys(block_table_stride, page_size, mask, window));
+  return MLA_OK;
+}
+
+int mla_indexer_fp8(int32_t num_heads, int32_t head_dim, int32_t page_size, int32_t num_pages, const void* q,
+                    const float* q_s, const uint32_t* input_row_offsets, int32_t batch, int32_t total_q,
+                    const void* k_cache, const float* k_scales, const int32_t* block_table,
+                    int32_t block_table_stride, const uint32_t* cache_lens, int32_t mask, int32_t window,
+                    int32_t top_k, int32_t* output_indices, double* output_scores, uint32_t flags,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_heads < 1 || head_dim < 1 || page_size < 1 || num_pages < 1 || batch < 1 || total_q < 0 ||
+      block_table_stride < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (mask < MLA_MASK_NULL || mask > MLA_MASK_SLIDING_WINDOW_CAUSAL) return MLA_ERR_INVALID_ARG;
+  if (mask == MLA_MASK_SLIDING_WINDOW_CAUSAL && window < 1) return MLA_ERR_INVALID_ARG;
+  if (top_k < 1) return MLA_ERR_INVALID_ARG;
+  if (top_k > kIndexerMaxTopK) return MLA_ERR_UNSUPPORTED;
+  if ((int64_t)num_pages * page_size > INT32_MAX || (int64_t)block_table_stride * page_size > INT32_MAX)
+    return MLA_ERR_UNSUPPORTED;
+  const size_t score_smem = (size_t)2 * num_heads * head_dim + (size_t)64 * head_dim + num_heads + 48 +
+                            (size_t)32 * num_heads * 8;
+  if (score_smem > kIndexerMaxScoreSmem) return MLA_ERR_UNSUPPORTED;
+  if (!q || !q_s || !input_row_offsets || !k_cache || !k_scales || !block_table || !cache_lens ||
+      !output_indices || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (flags & ~MLA_FLAG_DEBUG_CHECKS) return MLA_ERR_INVALID_ARG;
+  const int max_keys = indexer_max_keys(block_table_stride, page_size, mask, window);
+  if (workspace_bytes < indexer_workspace_bytes(total_q, max_keys) || !aligned16(workspace))
+    return MLA_ERR_WORKSPACE_TOO_SMALL;
+  PlanHeader* hdr = static_cast<PlanHeader*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), s) != cudaSuccess) return MLA_ERR_CUDA;
+  const cudaError_t e =
+      launch_indexer(num_heads, head_dim, page_size, num_pages, batch, total_q, mask, window, top_k,
+                     static_cast<const uint8_t*>(q), q_s, input_row_offsets, static_cast<const uint8_t*>(k_cache),
+                     k_scales, block_table, block_table_stride, cache_lens, max_keys, workspace, output_indices,
+                     output_scores, s);
+  if (e != cudaSuccess) {
+    std::fprintf(stderr, "mla_indexer_fp8: %s\n", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  if (flags & MLA_FLAG_DEBUG_CHECKS) return device_status(hdr, s);
+  return MLA_OK;
+}
+
 int mla_debug_wait_selftest(uint64_t limit_ns, void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < sizeof(PlanHeader) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   if (limit_ns == 0 || limit_ns > 1000000000ull) return MLA_ERR_INVALID_ARG;

@@ -63,4 +63,12 @@ cudaError_t launch_prologue(const mla_dims_t& d, void* q, const uint32_t* offset
                             const void* freqs, int max_seq_len, const void* gamma, float eps, PlanHeader* hdr,
                             cudaStream_t s);
 
+// The FP8 indexer: exact scores into the workspace, then per-token top_k selection.
+size_t indexer_workspace_bytes(int T, int max_keys);
+cudaError_t launch_indexer(int H, int D, int ps, int num_pages, int B, int T, int mask, int window, int top_k,
+                           const uint8_t* q, const float* q_s, const uint32_t* offsets, const uint8_t* k,
+                           const float* k_scales, const int32_t* block_table, int bt_stride,
+                           const uint32_t* cache_lens, int max_keys, void* workspace, int32_t* out_rows,
+                           double* out_scores, cudaStream_t s);
+
 }  // namespace mla
