@@ -51,8 +51,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["dsv3", "long", "long_swc", "fp8", "sparse"],
-                    default="dsv3")
+    ap.add_argument("--workload", choices=["dsv3", "long", "long_swc", "fp8", "sparse", "indexer",
+                                           "prologue"],
+                    default="dsv3",
+                    help="dsv3 is the headline; indexer and prologue time those entry points on "
+                         "the dsv3 batch shape")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0)
@@ -287,6 +290,127 @@ def run_reference(args, p):
     print(json.dumps(line), flush=True)
 
 
+def indexer_workload():
+    """The FP8 indexer on the dsv3 decode batch: 64 requests, lengths U[1024, 8192], 64 index
+    heads of depth 128 (DeepSeek-style lightning indexer), top 2048, causal."""
+    from workloads import mla as W
+    from workloads.indexer import make_indexer
+    lens = W.Stream(1001, "dsv3-lens").integers(1024, 8192, 64)
+    return make_indexer("indexer_dsv3", 1005, H=64, D=128, ps=64, cache_lens=lens, num_pages=6000,
+                        top_k=2048)
+
+
+def prologue_workload():
+    """The fused branch prologue on the dsv3 batch (the bf16 cache of config dsv3)."""
+    return make_workload("dsv3")
+
+
+# INT32 lane operations a second on this part (152 SMs x 128 lanes x max SM clock) and the
+# lane operations one exact e4m3 multiply-accumulate takes in the indexer's inner loop, as
+# written in the source (four byte loads, the significand product, the exponent sum, the
+# power of two and a 64-bit multiply-add)
+INT_LANE_OPS_PER_S = 152 * 128 * 2.07e9
+INDEXER_OPS_PER_MAC = 8
+
+
+def time_events(fn, flush, steps, warmup, stream):
+    import torch
+    for _ in range(max(3, warmup)):
+        flush.zero_()
+        fn()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(x.elapsed_time(y) for x, y in ev)
+
+
+def run_aux(args):
+    """Time the indexer or the prologue entry point; prints one JSON line."""
+    import numpy as np
+    import torch
+    import oracle
+    from mla_decode_attention_06_gb300 import build as libbuild
+    libbuild.build()
+    import mla_decode_attention_06_gb300 as M
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(device=dev, dtype=dt)
+    peaks, peak_kind = load_peaks()
+    clocks = ClockSampler(0)
+    if args.workload == "indexer":
+        p = indexer_workload()
+        d = dict(q=t(p.q, torch.uint8), q_s=t(p.q_s, torch.float32),
+                 off=t(p.row_offsets.astype(np.int32), torch.int32), k=t(p.k, torch.uint8),
+                 ks=t(p.k_scales, torch.float32), bt=t(p.block_table, torch.int32),
+                 lens=t(p.cache_lens.astype(np.int32), torch.int32))
+        out = torch.empty((p.T, p.top_k), dtype=torch.int32, device=dev)
+
+        def fn():
+            M.mla_indexer_fp8(d["q"], d["q_s"], d["off"], d["k"], d["ks"], d["bt"], d["lens"],
+                              page_size=p.ps, top_k=p.top_k, mask=p.mask, out=out)
+        ms = time_events(fn, flush, args.steps, args.warmup, stream)
+        keys = int(sum(int(n) for n in p.cache_lens))       # causal, one query per request
+        macs = keys * p.H * p.D
+        nbytes = keys * (p.D + 4) + p.T * p.H * (p.D + 4) + p.T * p.top_k * 4 + keys // p.ps * 4
+        achieved = macs * INDEXER_OPS_PER_MAC / (ms * 1e-3)
+        t0 = time.perf_counter()
+        oracle.indexer(p)
+        cpu_s = time.perf_counter() - t0
+        line = {"metric": "FP8 indexer us/call (exact e4m3 scores, top 2048)", "value": ms * 1e3,
+                "unit": "us/call", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": False, "dtype": "e4m3 -> exact int64 / f64",
+                "data": "synthetic (seeded)",
+                "config": {"workload": f"indexer: B={p.B}, H={p.H}, D={p.D}, keys={keys}, top_k={p.top_k}, "
+                                       "lengths U[1024, 8192], causal", "l2": "flushed before every step"},
+                "roofline": {"bound": "alu", "achieved": achieved, "peak": INT_LANE_OPS_PER_S,
+                             "unit": "int32 lane-op/s", "frac": achieved / INT_LANE_OPS_PER_S,
+                             "traffic": None, "note": f"{INDEXER_OPS_PER_MAC} lane ops per exact multiply-add; "
+                                                      f"HBM time of {nbytes / 1e6:.1f} MB is "
+                                                      f"{nbytes / (float(peaks['hbm_gbs']) * 1e9) * 1e6:.1f} us"},
+                "macs_per_call": macs, "gpu_launches": 2 * args.steps,
+                "cpu_baseline": {"value": cpu_s * 1e6, "unit": "us/call", "cores": oracle.num_threads(),
+                                 "kind": "oracle", "sample": "the whole call, one run"}}
+    else:
+        p = prologue_workload()
+        from workloads.run import device_inputs
+        dd = device_inputs(p, dev)
+        from workloads import mla as W
+        max_seq = int(p.cache_lens.max()) + 1
+        freqs = t(W.rope_freqs_cis(max_seq, p.R).view(np.int16), torch.int16).view(torch.bfloat16)
+        gamma = t(W.to_bf16_bits(np.ones(p.L)).view(np.int16), torch.int16).view(torch.bfloat16)
+        q = dd["q"].clone()
+        pool = dd["pool"]
+
+        def fn():
+            M.mla_branch_prologue(q, dd["offsets"], pool, dd["block_table"], dd["cache_lens"], freqs, gamma,
+                                  page_size=p.ps, kv_lora_rank=p.L, epsilon=1e-6)
+        ms = time_events(fn, flush, args.steps, args.warmup, stream)
+        nbytes = 2 * (p.T * p.H * p.R * 2) + 2 * p.T * (p.L + p.R) * 2 + p.T * p.R * 2 + p.L * 2
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        line = {"metric": "fused branch prologue us/call (RoPE + RMSNorm, in place)", "value": ms * 1e3,
+                "unit": "us/call", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": False, "dtype": "bf16 -> f64 -> bf16",
+                "data": "synthetic (seeded)",
+                "config": {"workload": workload_desc(p), "l2": "flushed before every step"},
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": float(peaks["hbm_gbs"]),
+                             "unit": "GB/s", "frac": achieved / float(peaks["hbm_gbs"]), "traffic": None,
+                             "note": "launch-bound: the call moves "
+                                     f"{nbytes / 1e6:.2f} MB"},
+                "gpu_launches": args.steps}
+    line["clocks"] = clocks.stop()
+    print(json.dumps(line), flush=True)
+
+
 def refuse_multi_gpu(args):
     """The GPU arm runs on one GPU only; under torchrun rank 0 says so and every rank exits."""
     n = max(args.gpus, world_size())
@@ -305,6 +429,13 @@ def main():
         refuse_multi_gpu(args)
         return
     if args.impl == "reference" and rank() != 0:
+        return
+    if args.workload in ("indexer", "prologue"):
+        if args.impl == "ours":
+            run_aux(args)
+        else:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the decode "
+                                                                  "workloads only"}), flush=True)
         return
     import numpy as np  # noqa: F401
     import torch

@@ -217,8 +217,8 @@ int mla_branch_prologue(const mla_dims_t* dims, void* q, const uint32_t* input_r
  *   workspace       mla_indexer_workspace_size() bytes, 16-byte aligned
  * Other arguments as mla_decode_paged.  Keys on a page id outside [0, num_pages)
  * are never read: they come out as -1 and are recorded (MLA_ERR_DEVICE_CHECK in
- * debug mode).  Shapes whose per-block scratch exceeds the limit
- * (2 H D + 64 D + 256 H bytes, about 200 KB) return MLA_ERR_UNSUPPORTED. */
+ * debug mode).  num_heads > 128, or shapes whose per-block scratch exceeds the
+ * limit ((H + 32)(D + 1) 4 + 256 H bytes, about 200 KB), return MLA_ERR_UNSUPPORTED. */
 int mla_indexer_workspace_size(int32_t total_q, int32_t block_table_stride, int32_t page_size, int32_t mask,
                                int32_t window, size_t* bytes);
 int mla_indexer_fp8(int32_t num_heads, int32_t head_dim, int32_t page_size, int32_t num_pages, const void* q,

@@ -406,9 +406,9 @@ int mla_indexer_fp8(int32_t num_heads, int32_t head_dim, int32_t page_size, int3
   if (top_k > kIndexerMaxTopK) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)num_pages * page_size > INT32_MAX || (int64_t)block_table_stride * page_size > INT32_MAX)
     return MLA_ERR_UNSUPPORTED;
-  const size_t score_smem = (size_t)2 * num_heads * head_dim + (size_t)64 * head_dim + num_heads + 48 +
+  const size_t score_smem = ((size_t)num_heads + 32) * (head_dim + 1) * 4 + num_heads + 48 +
                             (size_t)32 * num_heads * 8;
-  if (score_smem > kIndexerMaxScoreSmem) return MLA_ERR_UNSUPPORTED;
+  if (num_heads > 128 || score_smem > kIndexerMaxScoreSmem) return MLA_ERR_UNSUPPORTED;
   if (!q || !q_s || !input_row_offsets || !k_cache || !k_scales || !block_table || !cache_lens ||
       !output_indices || !workspace)
     return MLA_ERR_INVALID_ARG;

@@ -78,12 +78,12 @@ __device__ __forceinline__ bool token_range(const Args& a, int t, int& b, int& l
   return true;
 }
 
-// e4m3 (OCP E4M3FN) code -> value = sig * 2^(sh - 9), sig a signed integer <= 15, sh in 0..14.
-__device__ __forceinline__ void e4m3_parts(uint32_t c, int& sig, int& sh) {
+// e4m3 (OCP E4M3FN) code -> its value times 2^9, an integer: sig * 2^sh with the signed
+// significand sig (|sig| <= 15) and sh in 0..14, so |value * 2^9| < 2^18.
+__device__ __forceinline__ int e4m3_times_512(uint32_t c) {
   const int e = (c >> 3) & 15, m = c & 7;
-  const int mag = e ? (8 | m) : m;
-  sh = e ? e - 1 : 0;
-  sig = (c & 0x80u) ? -mag : mag;
+  const int mag = (e ? (8 | m) : m) << (e ? e - 1 : 0);
+  return (c & 0x80u) ? -mag : mag;
 }
 __device__ __forceinline__ bool e4m3_is_nan(uint32_t c) { return (c & 0x7Fu) == 0x7Fu; }
 
@@ -114,13 +114,12 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
   if (j0 >= n) return;
   const int nk = min(kKeysPerBlock, n - j0);
   const int HD = a.H * a.D;
-  int8_t* qsig = reinterpret_cast<int8_t*>(sm);          // [H * D]
-  int8_t* qsh = qsig + HD;                                // [H * D]
-  int8_t* ksig = qsh + HD;                                // [32 * D]
-  int8_t* ksh = ksig + kKeysPerBlock * a.D;               // [32 * D]
-  uint8_t* qnan = reinterpret_cast<uint8_t*>(ksh + kKeysPerBlock * a.D);   // [H]
-  uint8_t* knan = qnan + a.H;                                              // [32]
-  long long* dots = reinterpret_cast<long long*>(sm + (((size_t)2 * HD + 2 * kKeysPerBlock * a.D + a.H + kKeysPerBlock + 15) & ~(size_t)15));
+  const int DP = a.D + 1;                                  // padded rows: no bank conflicts
+  int* qv = reinterpret_cast<int*>(sm);                    // [H][DP] query values x 2^9
+  int* kv = qv + a.H * DP;                                 // [32][DP] key values x 2^9
+  uint8_t* qnan = reinterpret_cast<uint8_t*>(kv + kKeysPerBlock * DP);   // [H]
+  uint8_t* knan = qnan + a.H;                                            // [32]
+  long long* dots = reinterpret_cast<long long*>(sm + ((((size_t)a.H + kKeysPerBlock) * DP * 4 + a.H + kKeysPerBlock + 15) & ~(size_t)15));
   __shared__ long long rows_s[kKeysPerBlock];
   __shared__ int bad_s;
   if (tid == 0) bad_s = 0;
@@ -129,10 +128,7 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
   __syncthreads();
   for (int i = tid; i < HD; i += kScoreThreads) {
     const uint32_t c = a.q[(size_t)t * HD + i];
-    int sg, sh;
-    e4m3_parts(c, sg, sh);
-    qsig[i] = (int8_t)sg;
-    qsh[i] = (int8_t)sh;
+    qv[(i / a.D) * DP + i % a.D] = e4m3_times_512(c);
     if (e4m3_is_nan(c)) qnan[i / a.D] = 1;
   }
   if (tid < nk) {
@@ -144,27 +140,44 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
     rows_s[tid] = row;
   }
   __syncthreads();
-  for (int i = tid; i < nk * a.D; i += kScoreThreads) {
+  for (int i = tid; i < kKeysPerBlock * a.D; i += kScoreThreads) {
     const int key = i / a.D, d = i % a.D;
-    const long long row = rows_s[key];
+    const long long row = key < nk ? rows_s[key] : -1;
     const uint32_t c = row >= 0 ? a.k[(size_t)row * a.D + d] : 0u;
-    int sg, sh;
-    e4m3_parts(c, sg, sh);
-    ksig[i] = (int8_t)sg;
-    ksh[i] = (int8_t)sh;
-    if (e4m3_is_nan(c)) knan[key] = 1;
+    kv[key * DP + d] = e4m3_times_512(c);
+    if (key < nk && e4m3_is_nan(c)) knan[key] = 1;
   }
   __syncthreads();
-  // exact inner products, one (key, head) pair per thread at a time, in units of 2^-18
-  for (int p = tid; p < nk * a.H; p += kScoreThreads) {
-    const int key = p / a.H, h = p % a.H;
-    const int8_t* qs = qsig + h * a.D;
-    const int8_t* qe = qsh + h * a.D;
-    const int8_t* ks = ksig + key * a.D;
-    const int8_t* ke = ksh + key * a.D;
-    long long acc = 0;
-    for (int d = 0; d < a.D; ++d) acc += (long long)(qs[d] * ks[d]) * (1ll << (qe[d] + ke[d]));
-    dots[p] = acc;
+  // exact inner products in units of 2^-18 (each product below 2^36, sums in 64 bits):
+  // thread (kq, hq) holds keys kq and kq + 16 and heads hq, hq + 16, ... (a 2 x H/16 block)
+  {
+    const int kq = tid & 15, hq = tid >> 4;
+    const int nh = (a.H - hq + 15) / 16;                   // heads of this thread (<= 8)
+    long long acc[2][8];
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+      for (int y = 0; y < 8; ++y) acc[x][y] = 0;
+    const int* k0 = kv + kq * DP;
+    const int* k1 = kv + (kq + 16) * DP;
+    for (int d = 0; d < a.D; ++d) {
+      const long long x0 = k0[d], x1 = k1[d];
+#pragma unroll
+      for (int y = 0; y < 8; ++y) {
+        if (y < nh) {
+          const long long qy = qv[(hq + 16 * y) * DP + d];
+          acc[0][y] += x0 * qy;
+          acc[1][y] += x1 * qy;
+        }
+      }
+    }
+#pragma unroll
+    for (int y = 0; y < 8; ++y) {
+      if (y < nh) {
+        dots[kq * a.H + hq + 16 * y] = acc[0][y];
+        dots[(kq + 16) * a.H + hq + 16 * y] = acc[1][y];
+      }
+    }
   }
   __syncthreads();
   // head sum in head order, each product and sum rounded on its own
@@ -353,7 +366,7 @@ cudaError_t launch_indexer(int H, int D, int ps, int num_pages, int B, int T, in
   a.out_rows = out_rows;
   a.out_scores = out_scores;
   if (T == 0) return cudaSuccess;
-  const size_t s1 = (((size_t)2 * H * D + 2 * idx::kKeysPerBlock * D + H + idx::kKeysPerBlock + 15) & ~(size_t)15) +
+  const size_t s1 = ((((size_t)H + idx::kKeysPerBlock) * (D + 1) * 4 + H + idx::kKeysPerBlock + 15) & ~(size_t)15) +
                     (size_t)idx::kKeysPerBlock * H * 8;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(idx::scores_kernel), (int)s1);
   if (e != cudaSuccess) return e;

@@ -10,12 +10,16 @@
 //     RMSNorm of its latent part, c / sqrt(mean(c^2) + eps) * gamma, and the
 //     same rotation of its rope part;
 //   - nothing else changes.
-// Every value is computed in double precision from the bf16 inputs, with each
-// product and sum rounded on its own (no fused multiply-add) in the order
-// written above, and rounded once to bf16 (nearest, ties to even).  The mean
-// square is summed in latent order by one thread.  So the results do not depend
-// on the launch shape, and they are the exactly rounded values of those
-// expressions.
+// Every result is the bf16 (nearest, ties to even) of the expression's value:
+//   - rotations: the two products of bf16 values are exact in fp32 and their
+//     difference / sum is formed exactly as an fp32 pair (TwoSum), which is
+//     rounded to bf16 once, looking at the low part only at a halfway point; the
+//     result is the exactly rounded value of x0 c - x1 s (x0 s + x1 c), as a
+//     double-precision evaluation gives it;
+//   - RMSNorm: the mean square, 1 / sqrt(mean + eps) and the two products are
+//     double precision; the mean square is summed by a tree (the double-precision
+//     sums of any order differ in the last bits only, far below the bf16 rounding
+//     step), the products rounded on their own, the result rounded once to bf16.
 //
 // One block per query token: its threads share the token's heads and the row.
 #include <cstdio>
@@ -72,17 +76,49 @@ __device__ __forceinline__ uint16_t round_bf16(double x) {
   return (uint16_t)(sign | (bexp << 7) | bman);
 }
 
+__device__ __forceinline__ float bff(const __nv_bfloat16 v) {
+  return __uint_as_float(((uint32_t)__bfloat16_as_ushort(v)) << 16);
+}
+
+// bf16 bits of the exact sum hi + lo, where (hi, lo) is a TwoSum pair (hi = fl(hi + lo),
+// |lo| at most half an fp32 ulp of hi): nearest, ties to even.  Only when hi lies
+// exactly halfway between two bf16 values does lo decide the direction.
+__device__ __forceinline__ uint16_t round_bf16_pair(float hi, float lo) {
+  const uint32_t u = __float_as_uint(hi);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0;                // NaN
+  const uint32_t sign = u & 0x80000000u, mag = u & 0x7FFFFFFFu;
+  const uint32_t rem = mag & 0xFFFFu, base = mag >> 16;
+  bool up;
+  if (rem != 0x8000u) {
+    up = rem > 0x8000u;
+  } else {
+    const float away = sign ? -lo : lo;                                 // lo along hi's direction
+    up = away > 0.f || (away == 0.f && (base & 1u));
+  }
+  return (uint16_t)((sign >> 16) | (base + (up ? 1u : 0u)));
+}
+
+// (a + b) as an exact pair: hi = fl(a + b), lo = the rounding error (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float& hi, float& lo) {
+  hi = __fadd_rn(a, b);
+  const float z = __fsub_rn(hi, a);
+  lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, z)), __fsub_rn(b, z));
+}
+
+// (x0, x1) turned by (c, s): the products of bf16 values are exact in fp32.
 __device__ __forceinline__ void rotate(__nv_bfloat16* x, const __nv_bfloat16* f) {
-  const double x0 = bf(x[0]), x1 = bf(x[1]), c = bf(f[0]), s = bf(f[1]);
-  const uint16_t y0 = round_bf16(__dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s)));
-  const uint16_t y1 = round_bf16(__dadd_rn(__dmul_rn(x0, s), __dmul_rn(x1, c)));
-  x[0] = __ushort_as_bfloat16(y0);
-  x[1] = __ushort_as_bfloat16(y1);
+  const float x0 = bff(x[0]), x1 = bff(x[1]), c = bff(f[0]), s = bff(f[1]);
+  float h0, l0, h1, l1;
+  two_sum(__fmul_rn(x0, c), -__fmul_rn(x1, s), h0, l0);
+  two_sum(__fmul_rn(x0, s), __fmul_rn(x1, c), h1, l1);
+  x[0] = __ushort_as_bfloat16(round_bf16_pair(h0, l0));
+  x[1] = __ushort_as_bfloat16(round_bf16_pair(h1, l1));
 }
 
 __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   __shared__ double s_inv;
   __shared__ double s_lat[kMaxLatent];
+  __shared__ double s_part[kThreads / 32];
   const int t = blockIdx.x, tid = threadIdx.x;
   // request of token t: the last b with offsets[b] <= t
   int lo = 0, hi = a.B - 1;
@@ -110,13 +146,20 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
     const int h = i / (a.R / 2), pr = i % (a.R / 2);
     rotate(a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr, f + 2 * pr);
   }
-  // the row: latent values into shared memory, mean square summed in order by one thread
+  // the row: latent values into shared memory, mean square summed by a tree
   __nv_bfloat16* rp = a.pool + (size_t)row * (a.L + a.R);
-  for (int l = tid; l < a.L; l += kThreads) s_lat[l] = bf(rp[l]);
+  double part = 0.0;
+  for (int l = tid; l < a.L; l += kThreads) {
+    const double v = bf(rp[l]);
+    s_lat[l] = v;
+    part = __dadd_rn(part, __dmul_rn(v, v));
+  }
+  for (int o = 16; o > 0; o >>= 1) part = __dadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+  if ((tid & 31) == 0) s_part[tid >> 5] = part;
   __syncthreads();
   if (tid == 0) {
     double ms = 0.0;
-    for (int l = 0; l < a.L; ++l) ms = __dadd_rn(ms, __dmul_rn(s_lat[l], s_lat[l]));
+    for (int w = 0; w < kThreads / 32; ++w) ms = __dadd_rn(ms, s_part[w]);
     s_inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ms, (double)a.L), a.eps)));
   }
   __syncthreads();
