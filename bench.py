@@ -51,27 +51,36 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["dsv3", "long", "long_swc", "fp8", "sparse", "indexer",
-                                           "prologue"],
+    ap.add_argument("--workload", choices=["dsv3", "dsv3_mtp", "long", "long_swc", "fp8", "sparse",
+                                           "sparse_mtp", "indexer", "prologue"],
                     default="dsv3",
                     help="dsv3 is the headline; indexer and prologue time those entry points on "
                          "the dsv3 batch shape")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0)
+    walk = ap.add_mutually_exclusive_group()
+    walk.add_argument("--fold-pairs", action="store_true",
+                      help="walk consecutive query tokens of a request in pairs (one tile load for both)")
+    walk.add_argument("--per-token", action="store_true",
+                      help="walk every query token on its own")
     ap.add_argument("--profile-case", action="store_true",
-                    help="a smaller dsv3 case for ncu captures: batch 32 over an 8192-page pool "
-                         "(170 MB of attended cache, above the L2 size)")
+                    help="a smaller case of the workload for ncu captures (dsv3: batch 32 over an "
+                         "8192-page pool, 170 MB of attended cache, above the L2 size)")
     return ap.parse_args()
 
 
 def make_workload(name, profile_case=False):
     from workloads import mla as W
     if profile_case:
-        return W.config_dsv3(B=32, num_pages=8192)
-    return {"dsv3": W.config_dsv3, "long": W.config_long,
+        # smaller cases of the same shapes for ncu captures (inputs still above the L2 size)
+        return {"dsv3": lambda: W.config_dsv3(B=32, num_pages=8192),
+                "dsv3_mtp": lambda: W.config_dsv3_mtp(B=16),
+                "fp8": lambda: W.config_fp8(B=32),
+                "sparse": lambda: W.config_sparse(B=48)}[name]()
+    return {"dsv3": W.config_dsv3, "dsv3_mtp": W.config_dsv3_mtp, "long": W.config_long,
             "long_swc": lambda: W.config_long(window=4096), "fp8": W.config_fp8,
-            "sparse": W.config_sparse}[name]()
+            "sparse": W.config_sparse, "sparse_mtp": W.config_sparse_mtp}[name]()
 
 
 def workload_desc(p):
@@ -82,12 +91,14 @@ def workload_desc(p):
 
 
 def key_counts(p):
-    """Attended keys per query token (the units of the decode kernel)."""
+    """Attended keys per query token (the units of the decode's arithmetic)."""
     import numpy as np
     if p.sparse:
         cnt = np.minimum(p.topk_lengths if p.topk_lengths is not None
                          else np.full(p.B, p.indices.shape[1]), p.indices.shape[1])
-        return np.array([int((p.indices[b, :cnt[b]] >= 0).sum()) for b in range(p.B)])
+        per_req = np.array([int((p.indices[b, :cnt[b]] >= 0).sum()) for b in range(p.B)])
+        req = np.repeat(np.arange(p.B), np.diff(p.row_offsets.astype(np.int64)))
+        return per_req[req]
     req, pos = p.query_positions()
     lens = p.cache_lens[req].astype(np.int64)
     if p.mask == 0:
@@ -97,12 +108,36 @@ def key_counts(p):
     return hi - lo
 
 
+def rows_read(p):
+    """Cache rows the method must read: per request, the union of its tokens' key sets
+    (a request's query tokens share its cached rows)."""
+    import numpy as np
+    if p.sparse:
+        cnt = np.minimum(p.topk_lengths if p.topk_lengths is not None
+                         else np.full(p.B, p.indices.shape[1]), p.indices.shape[1])
+        return int(sum(int((p.indices[b, :cnt[b]] >= 0).sum()) for b in range(p.B))), 0
+    req, pos = p.query_positions()
+    hi = pos + 1 if p.mask != 0 else p.cache_lens[req].astype(np.int64)
+    lo = np.maximum(0, pos + 1 - p.window) if p.mask == 2 else np.zeros_like(hi)
+    rows, pages = 0, 0
+    for b in range(p.B):
+        sel = req == b
+        if not sel.any():
+            continue
+        a, e = int(lo[sel].min()), int(hi[sel].max())
+        if e > a:
+            rows += e - a
+            pages += (e - 1) // p.ps - a // p.ps + 1
+    return rows, pages
+
+
 def algorithmic(p):
     """Bytes and FLOPs the call must move / compute (workspace excluded)."""
     keys = int(key_counts(p).sum())
+    rows, pages = rows_read(p)
     row = p.row_bytes + (4 if p.kv_fmt == "fp8" else 0)
-    kv_bytes = keys * row
-    idx_bytes = (keys * 4) if p.sparse else int(sum(math.ceil(k / p.ps) for k in key_counts(p)) * 4)
+    kv_bytes = rows * row
+    idx_bytes = (rows * 4) if p.sparse else pages * 4
     wb = 1 if p.w_fmt == "fp8" else 2
     w_bytes = p.H * p.L * p.N * wb + p.H * p.V * p.L * wb
     if p.w_fmt == "fp8":
@@ -192,12 +227,31 @@ def rank():
     return int(os.environ.get("RANK", "0"))
 
 
+def walk_arg(args):
+    """The binding's fold_pairs argument: None leaves the query walk to the library."""
+    if getattr(args, "fold_pairs", False):
+        return True
+    if getattr(args, "per_token", False):
+        return False
+    return None
+
+
+def folds(p, args) -> bool:
+    """Whether the library walks this call's query tokens in pairs (the rule of
+    MLA_FLAG_FOLD_PAIRS / MLA_FLAG_PER_TOKEN in include/mla_decode.h)."""
+    if p.T < 2 * p.B or p.kv_fmt != "bf16" or p.L != 512 or p.R != 64:
+        return False
+    w = walk_arg(args)
+    return p.sparse if w is None else w
+
+
 def config_of(p, args):
     """The workload description both arms print (identical keys and values)."""
     return {"workload": workload_desc(p), "global_batch": p.B, "query_tokens": p.T,
             "parallelism": "single GPU",
             "l2": "GPU arm: a 2 x L2-size buffer is written before every timed step",
-            "num_splits": args.num_splits or "auto"}
+            "num_splits": args.num_splits or "auto",
+            "query_walk": "folded pairs" if folds(p, args) else "one token at a time"}
 
 
 def oracle_call_seconds(p):
@@ -246,8 +300,8 @@ def cpu_baseline(p):
             "cpu_model": cpu_model()}
 
 
-WORKLOAD_OF = {"dsv3_bf16": "dsv3", "long": "long", "long_swc": "long_swc", "fp8": "fp8",
-               "sparse": "sparse"}
+WORKLOAD_OF = {"dsv3_bf16": "dsv3", "dsv3_mtp": "dsv3_mtp", "long": "long", "long_swc": "long_swc",
+               "fp8": "fp8", "sparse": "sparse", "sparse_mtp": "sparse_mtp"}
 
 
 def cpu_model():
@@ -463,7 +517,7 @@ def main():
 
     def step(timing=False, on_stream=None):
         run_gpu(p, d, num_splits=args.num_splits, out=out, lse_out=lse, workspace=ws,
-                stream=on_stream or stream, timing=timing)
+                stream=on_stream or stream, timing=timing, fold_pairs=walk_arg(args))
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -587,7 +641,7 @@ def e2e(p, d, args, dev, out, lse, ws, flush, stream):
             dd[k] = d[k]
             dd[k].copy_(t, non_blocking=True)
         run_gpu(p, dd, num_splits=args.num_splits, out=out, lse_out=None, workspace=ws,
-                stream=stream, want_lse=False)
+                stream=stream, want_lse=False, fold_pairs=walk_arg(args))
         out_h.copy_(out, non_blocking=True)
         e.record(stream)
         e.synchronize()

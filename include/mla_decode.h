@@ -75,6 +75,20 @@ typedef enum {
 /* Record a CUDA event pair around every kernel of the call; read the durations
  * with mla_decode_kernel_times() once the stream has finished. */
 #define MLA_FLAG_KERNEL_TIMING 2u
+/* Query walk.  Consecutive query tokens of a request can be walked in pairs
+ * (decode page: fold_shared_index; a request's tokens share its cache rows or
+ * index list): every cache tile is read once for both tokens by a cluster of
+ * four CTAs.  Pairs are possible when the call has at least two query tokens
+ * per request on average (total_q >= 2 * batch) and a bf16 cache with
+ * (L, R) = (512, 64); otherwise every token is walked on its own.  Where
+ * possible, the default folds sparse calls (whose gathered row loads bound the
+ * main loop: folding halves them) and walks dense calls one token at a time
+ * (their main loop is bound by each CTA's score contraction, which folding
+ * does not shrink, and a cluster of four leaves SMs idle).  MLA_FLAG_FOLD_PAIRS
+ * forces pairs, MLA_FLAG_PER_TOKEN forces one token at a time; setting both is
+ * an invalid argument.  The two walks agree to rounding. */
+#define MLA_FLAG_FOLD_PAIRS 4u
+#define MLA_FLAG_PER_TOKEN 8u
 
 /* Problem dimensions (decode page: q [.., num_heads, q_head_size];
  * mla_decode_branch_fp8 page: w_uk [num_heads, kv_latent_dim, qk_nope_head_dim],
@@ -94,16 +108,22 @@ typedef struct {
   int32_t mask;          /* mla_mask_t */
   int32_t window;        /* tokens, >= 1 for SLIDING_WINDOW_CAUSAL, ignored otherwise */
   float scale;           /* multiplies q.k, usually 1/sqrt(N + R) */
-  int32_t num_splits;    /* KV partitions; 0 = one per pair of SMs.  The call cuts the
+  int32_t num_splits;    /* KV partitions; 0 = as many as the device keeps resident at
+                            once (one cluster of two CTAs each, four when query tokens
+                            are walked in pairs), at most one per pair (four) of SMs,
+                            from the CUDA occupancy query.  The call cuts the
                             batch's key tiles into that many partitions of about equal
                             cost (tiles plus a charge per query token started); a token
                             cut between partitions is merged in the decode kernel. */
-  uint32_t flags;        /* MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_KERNEL_TIMING */
+  uint32_t flags;        /* MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_KERNEL_TIMING |
+                            MLA_FLAG_FOLD_PAIRS | MLA_FLAG_PER_TOKEN */
 } mla_opts_t;
 
 /* Bytes of scratch a call needs for `total_q` query tokens with these dims and
  * opts (num_splits decides the partial-result slots).  Uses the current
- * device's SM count when opts->num_splits == 0.  Writes *bytes. */
+ * device's SM count when opts->num_splits == 0.  The size covers both query
+ * walks (one token at a time and, where it applies, folded pairs) whatever
+ * opts->flags says, so one workspace serves calls with either.  Writes *bytes. */
 int mla_decode_workspace_size(const mla_dims_t* dims, const mla_opts_t* opts, int32_t batch,
                               int32_t total_q, size_t* bytes);
 

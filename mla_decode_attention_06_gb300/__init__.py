@@ -21,7 +21,8 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import (MLA_FLAG_DEBUG_CHECKS, MLA_FLAG_KERNEL_TIMING, MLA_MASK_CAUSAL, MLA_MASK_NULL,
+from ._lib import (MLA_FLAG_DEBUG_CHECKS, MLA_FLAG_KERNEL_TIMING, MLA_FLAG_FOLD_PAIRS, MLA_FLAG_PER_TOKEN,
+                   MLA_MASK_CAUSAL, MLA_MASK_NULL,
                    MLA_MASK_SLIDING_WINDOW_CAUSAL, MlaDims, MlaError, MlaOpts, kernel_times)
 
 __all__ = ["mla_decode_paged", "mla_decode_paged_fp8", "mla_decode_sparse", "mla_branch_prologue",
@@ -50,8 +51,10 @@ def _ptr(t: Optional[torch.Tensor], name: str, dtypes=None, device=None):
     return t.data_ptr()
 
 
-def _opts(mask, window, scale, num_splits, debug, timing=False) -> MlaOpts:
-    flags = (MLA_FLAG_DEBUG_CHECKS if debug else 0) | (MLA_FLAG_KERNEL_TIMING if timing else 0)
+def _opts(mask, window, scale, num_splits, debug, timing=False, fold_pairs=None) -> MlaOpts:
+    # fold_pairs: None = the library's choice, True / False = force pairs / one token at a time
+    walk = 0 if fold_pairs is None else (MLA_FLAG_FOLD_PAIRS if fold_pairs else MLA_FLAG_PER_TOKEN)
+    flags = (MLA_FLAG_DEBUG_CHECKS if debug else 0) | (MLA_FLAG_KERNEL_TIMING if timing else 0) | walk
     return MlaOpts(mask=int(mask), window=int(window), scale=float(scale),
                    num_splits=int(num_splits), flags=flags)
 
@@ -95,7 +98,8 @@ def _stream(stream, device):
 def mla_decode_paged(q, input_row_offsets, kv_pool, block_table, cache_lens, w_uk, w_uv, *,
                      page_size: int, scale: Optional[float] = None, mask: int = MLA_MASK_CAUSAL,
                      window: int = 0, num_splits: int = 0, debug: bool = False, out=None,
-                     lse_out=None, workspace=None, stream=None, timing: bool = False):
+                     lse_out=None, workspace=None, stream=None, timing: bool = False,
+                     fold_pairs: Optional[bool] = None):
     """Dense bf16 decode.  Shapes as in include/mla_decode.h: q [T,H,N+R] bf16,
     input_row_offsets uint32/int32 [B+1], kv_pool bf16 (any shape, page-major rows of
     L+R), block_table int32 [B, stride], cache_lens uint32/int32 [B], w_uk [H,L,N],
@@ -104,7 +108,7 @@ def mla_decode_paged(q, input_row_offsets, kv_pool, block_table, cache_lens, w_u
     B = input_row_offsets.numel() - 1
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[2])
-    opts = _opts(mask, window, scale, num_splits, debug, timing)
+    opts = _opts(mask, window, scale, num_splits, debug, timing, fold_pairs)
     dims, out, workspace = _prepare(q, w_uk, w_uv, page_size,
                                     kv_pool.numel() * kv_pool.element_size(),
                                     lambda L, R: 2 * (L + R), out, lse_out, workspace, opts, B)
@@ -128,14 +132,14 @@ def mla_decode_paged_fp8(q, input_row_offsets, kv_pool_fp8, kv_scales, block_tab
                          scale: Optional[float] = None, mask: int = MLA_MASK_CAUSAL,
                          window: int = 0, num_splits: int = 0, debug: bool = False, out=None,
                          lse_out=None, workspace=None, stream=None, q_scale=None,
-                         timing: bool = False):
+                         timing: bool = False, fold_pairs: Optional[bool] = None):
     """FP8 latent cache: kv_pool_fp8 uint8 rows [L e4m3 | R bf16], kv_scales f32 [rows],
     e4m3 weights (uint8 or float8_e4m3fn) with fp32 128x128 block scales."""
     dev = q.device
     B = input_row_offsets.numel() - 1
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[2])
-    opts = _opts(mask, window, scale, num_splits, debug, timing)
+    opts = _opts(mask, window, scale, num_splits, debug, timing, fold_pairs)
     dims, out, workspace = _prepare(q, w_uk_fp8, w_uv_fp8, page_size,
                                     kv_pool_fp8.numel() * kv_pool_fp8.element_size(),
                                     lambda L, R: L + 2 * R, out, lse_out, workspace, opts, B)
@@ -161,14 +165,14 @@ def mla_decode_paged_fp8(q, input_row_offsets, kv_pool_fp8, kv_scales, block_tab
 def mla_decode_sparse(q, input_row_offsets, kv_pool, d_indices, topk_lengths, w_uk, w_uv, *,
                       page_size: int, scale: Optional[float] = None, num_splits: int = 0,
                       debug: bool = False, out=None, lse_out=None, workspace=None, stream=None,
-                      timing: bool = False):
+                      timing: bool = False, fold_pairs: Optional[bool] = None):
     """Sparse top-k decode over physical rows d_indices int32 [B, stride] (-1 = skip);
     topk_lengths int32 [B] or None."""
     dev = q.device
     B = input_row_offsets.numel() - 1
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[2])
-    opts = _opts(MLA_MASK_NULL, 0, scale, num_splits, debug, timing)
+    opts = _opts(MLA_MASK_NULL, 0, scale, num_splits, debug, timing, fold_pairs)
     dims, out, workspace = _prepare(q, w_uk, w_uv, page_size,
                                     kv_pool.numel() * kv_pool.element_size(),
                                     lambda L, R: 2 * (L + R), out, lse_out, workspace, opts, B)

@@ -23,6 +23,8 @@ MLA_MASK_CAUSAL = 1
 MLA_MASK_SLIDING_WINDOW_CAUSAL = 2
 MLA_FLAG_DEBUG_CHECKS = 1
 MLA_FLAG_KERNEL_TIMING = 2
+MLA_FLAG_FOLD_PAIRS = 4
+MLA_FLAG_PER_TOKEN = 8
 KERNEL_NAMES = ("absorb_w_uk", "decode_splitkv", "w_uv")
 
 EXPORTED = ("mla_decode_workspace_size", "mla_decode_paged", "mla_decode_paged_fp8",

@@ -66,7 +66,24 @@ int check_dims(const mla_dims_t* d) {
   return MLA_OK;
 }
 
-int resolve_splits(const mla_opts_t* o, int* K) {
+// Query tokens are walked in pairs (two consecutive tokens of a request share
+// every cache tile they read, one tile load serving both) when the batch has at
+// least two tokens per request on average, the shape has a folded instance, and
+// either the caller asks for pairs or, by default, the call is sparse (its
+// gathered loads bound the main loop; a dense call's tile period is set by the
+// score contraction, which pairs do not shrink).
+bool use_fold(const mla_dims_t* d, const mla_opts_t* o, int batch, int total_q, bool fp8_cache, bool sparse) {
+  if (total_q < 2 * batch || !decode_fold_supported(*d, fp8_cache)) return false;
+  if (o->flags & MLA_FLAG_FOLD_PAIRS) return true;
+  if (o->flags & MLA_FLAG_PER_TOKEN) return false;
+  return sparse;
+}
+
+// The partition count: the caller's, else as many partitions as the device runs at
+// once for the instance the call uses (`d` given), or, for sizing the workspace, the
+// SM count over the CTAs per partition, which is never below that.
+int resolve_splits(const mla_opts_t* o, bool fold, int* K, const mla_dims_t* d = nullptr, bool fp8 = false,
+                   bool sparse = false) {
   if (o->num_splits < 0 || o->num_splits > kMaxSplits) return MLA_ERR_INVALID_ARG;
   if (o->num_splits > 0) {
     *K = o->num_splits;
@@ -75,7 +92,10 @@ int resolve_splits(const mla_opts_t* o, int* K) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MLA_ERR_CUDA;
-  *K = sms / 2 > 0 ? sms / 2 : 1;
+  const int per = fold ? 4 : 2;   // CTAs per partition (one for narrow latents, which stay at sms / 2)
+  const int bound = sms / per > 0 ? sms / per : 1;
+  int n = d ? decode_default_partitions(*d, fold, fp8, sparse) : 0;
+  *K = n > 0 && n <= bound ? n : bound;
   return MLA_OK;
 }
 
@@ -84,7 +104,9 @@ int check_opts(const mla_opts_t* o) {
   if (o->mask < MLA_MASK_NULL || o->mask > MLA_MASK_SLIDING_WINDOW_CAUSAL) return MLA_ERR_INVALID_ARG;
   if (o->mask == MLA_MASK_SLIDING_WINDOW_CAUSAL && o->window < 1) return MLA_ERR_INVALID_ARG;
   if (!(o->scale == o->scale)) return MLA_ERR_INVALID_ARG;   // NaN
-  if (o->flags & ~(MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_KERNEL_TIMING)) return MLA_ERR_INVALID_ARG;
+  if (o->flags & ~(MLA_FLAG_DEBUG_CHECKS | MLA_FLAG_KERNEL_TIMING | MLA_FLAG_FOLD_PAIRS | MLA_FLAG_PER_TOKEN))
+    return MLA_ERR_INVALID_ARG;
+  if ((o->flags & MLA_FLAG_FOLD_PAIRS) && (o->flags & MLA_FLAG_PER_TOKEN)) return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
 
@@ -136,9 +158,11 @@ int run(const CallCommon& c) {
   if (!aligned16(c.q) || !aligned16(c.kv_pool) || !aligned16(c.w_uk) || !aligned16(c.w_uv) ||
       !aligned16(c.out) || !aligned16(c.ws))
     return MLA_ERR_INVALID_ARG;
+  const bool sparse = c.ks.indices != nullptr;
+  const bool fold = use_fold(c.d, c.o, c.B, c.T, c.kv_fmt == KVFmt::kE4M3, sparse);
   int K = 0;
-  if ((st = resolve_splits(c.o, &K))) return st;
-  const WorkspaceLayout lay = workspace_layout(*c.d, c.T, K);
+  if ((st = resolve_splits(c.o, fold, &K, c.d, c.kv_fmt == KVFmt::kE4M3, sparse))) return st;
+  const WorkspaceLayout lay = workspace_layout(*c.d, c.T, K, fold ? 2 : 1);
   if (c.ws_bytes < lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
 
   char* ws = static_cast<char*>(c.ws);
@@ -166,6 +190,7 @@ int run(const CallCommon& c) {
   a.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   a.counters = reinterpret_cast<int*>(ws + lay.counters);
   a.bounds = reinterpret_cast<const int*>(ws + lay.bounds);
+  a.fold = fold;
   PlanInputs pin{};
   pin.offsets = c.offsets;
   pin.B = c.B;
@@ -182,6 +207,7 @@ int run(const CallCommon& c) {
   pin.lse_ws = a.lse_ws;
   pin.H = c.d->num_heads;
   pin.L = c.d->kv_lora_rank;
+  pin.fold = fold;
 
   EventSet* timer = nullptr;
   if (c.o->flags & MLA_FLAG_KERNEL_TIMING) {
@@ -221,9 +247,18 @@ int mla_decode_workspace_size(const mla_dims_t* dims, const mla_opts_t* opts, in
   int st = check_dims(dims);
   if (st) return st;
   if (!opts || !bytes || batch < 1 || total_q < 0) return MLA_ERR_INVALID_ARG;
+  // one size for both walks, whether or not opts asks for folded pairs; the bf16
+  // shapes' size also covers an e4m3 cache (whose calls never fold)
+  mla_opts_t both = *opts;
+  both.flags |= MLA_FLAG_FOLD_PAIRS;
+  const bool fold = use_fold(dims, &both, batch, total_q, false, false);
   int K = 0;
-  if ((st = resolve_splits(opts, &K))) return st;
-  *bytes = workspace_layout(*dims, total_q, K).total;
+  if ((st = resolve_splits(opts, fold, &K))) return st;
+  const size_t a = workspace_layout(*dims, total_q, K, fold ? 2 : 1).total;
+  int K1 = 0;
+  if ((st = resolve_splits(opts, false, &K1))) return st;
+  const size_t b = workspace_layout(*dims, total_q, K1, 1).total;
+  *bytes = a > b ? a : b;
   return MLA_OK;
 }
 

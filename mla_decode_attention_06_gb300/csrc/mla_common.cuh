@@ -20,6 +20,12 @@ constexpr int kDeviceTimeout = 2;
 // Keys are processed in tiles of kTileKeys aligned to logical position 0, so
 // the token covers tiles [tile_first, tile_first + ntiles); across all tokens
 // its tiles occupy the global tile interval [tile_start, tile_start + ntiles).
+//
+// When a call folds the query tokens of a request in pairs (two consecutive
+// tokens of one request share every cache tile they read), the first token of
+// a pair leads: [lo, hi) and its tiles cover the union of both tokens' key
+// ranges and ntok = 2; the second token follows: no tiles of its own (ntiles =
+// 0, ntok = 0).  [mlo, mhi) is always the token's own key range (its mask).
 struct TokenPlan {
   int32_t b;
   int32_t lo, hi;
@@ -27,6 +33,9 @@ struct TokenPlan {
   int32_t tile_start;
   int32_t ntiles;
   int32_t part_first, part_last;   // the KV partitions holding its first / last tile
+  int32_t mlo, mhi;                // the token's own key range
+  int32_t ntok;                    // tokens walked with these tiles: 1, 2 (a pair's first) or 0
+  int32_t pad;
 };
 
 struct PlanHeader {
@@ -57,14 +66,15 @@ struct KeySource {
 //   q_full     bf16 [T, 128, L+R]: absorbed queries, rows h >= H zero
 //   o_lat      bf16 [T, H, L]: normalised latent outputs
 //   lse        fp32 [T, H]
-//   part_o     fp32 [K, 2, H, L]: partials of the first / last segment of each partition
-//   part_lse   fp32 [K, 2, 2, H]: their log-sum-exp, one copy per cluster rank
+//   part_o     fp32 [K, 2 * NI, H, L]: partials of the first / last segment of each
+//              partition, NI token slots each (2 when tokens are folded in pairs)
+//   part_lse   fp32 [K, 2 * NI, 2, H]: their log-sum-exp, one copy per latent half
 struct WorkspaceLayout {
   size_t header, plan, counters, bounds, q_full, o_lat, lse, part_o, part_lse, total;
 };
 
-// Host-side: the layout for T tokens and K KV partitions.
-inline WorkspaceLayout workspace_layout(const mla_dims_t& d, int T, int K) {
+// Host-side: the layout for T tokens, K KV partitions and NI token slots per partial.
+inline WorkspaceLayout workspace_layout(const mla_dims_t& d, int T, int K, int NI = 1) {
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   WorkspaceLayout w{};
   size_t o = 0;
@@ -75,8 +85,8 @@ inline WorkspaceLayout workspace_layout(const mla_dims_t& d, int T, int K) {
   w.q_full = o;  o = up(o + (size_t)T * kMaxHeads * (d.kv_lora_rank + d.qk_rope) * 2);
   w.o_lat = o;   o = up(o + (size_t)T * d.num_heads * d.kv_lora_rank * 2);
   w.lse = o;     o = up(o + (size_t)T * d.num_heads * 4);
-  w.part_o = o;  o = up(o + (size_t)K * 2 * d.num_heads * d.kv_lora_rank * 4);
-  w.part_lse = o; o = up(o + (size_t)K * 2 * 2 * d.num_heads * 4);   // [K, slot, cta rank, H]
+  w.part_o = o;  o = up(o + (size_t)K * 2 * NI * d.num_heads * d.kv_lora_rank * 4);
+  w.part_lse = o; o = up(o + (size_t)K * 2 * NI * 2 * d.num_heads * 4);   // [K, slot, latent half, H]
   w.total = o;
   return w;
 }

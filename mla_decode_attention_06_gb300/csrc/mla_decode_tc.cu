@@ -80,7 +80,7 @@ struct Smem {   // control block after the stage ring
   uint64_t conv_sync;            // converters: every code read before the overlapping rows are written
   uint64_t fix_bar, fix_done;    // softmax: partial written / claim outcome published
   uint64_t mrg_full[2], mrg_done[2];   // merge: a half partial landed in its buffer / was read
-  uint64_t bye;                  // the peer CTA is done touching this CTA's shared memory
+  uint64_t bye;                  // the other CTAs are done touching this CTA's shared memory
   int32_t rowid[kMaxStages][64]; // physical row of each tile row (kLoadFp8, kLoadSparse)
   uint32_t tmem_base;
   int abort;
@@ -90,12 +90,17 @@ struct Smem {   // control block after the stage ring
 template <int kLatentPerCta, int kCluster, int kMode>
 struct Cfg {
   static constexpr int CL = kCluster;
+  // A cluster of four folds two query tokens of a request: CTA r takes token slot
+  // r / 2 and latent half r % 2; every cache tile is multicast to all four.
+  static constexpr int NHALF = CL == 4 ? 2 : CL;    // latent slices of O in the cluster
+  static constexpr int NSLOT = CL == 4 ? 2 : 1;     // query tokens walked together
+  static constexpr int kMcMask = (1 << CL) - 1;     // every CTA of the cluster
   static constexpr int LC = kLatentPerCta;          // latent columns of O owned by one CTA
-  static constexpr int L = LC * CL;                 // latent width
+  static constexpr int L = LC * NHALF;              // latent width
   static constexpr int NLB = L / 64;                // 64-column latent boxes per cached row
   static constexpr int kBox = 64 * 128;             // one 128B-swizzled box: 64 rows x 128 B
   static constexpr int kStageBytes = (NLB + 1) * kBox;   // latent boxes + one rope box
-  static constexpr int kStages = CL == 2 ? 2 : kMaxStages;
+  static constexpr int kStages = CL >= 2 ? 2 : kMaxStages;
   static constexpr int QT = L < 256 ? L : 256;      // latent columns of the query held in TMEM
   static constexpr int NQS = (L - QT) / 64;         // latent boxes of the query in shared memory
   static constexpr int kQBox = 128 * 128;           // 128 rows x 128 B
@@ -113,10 +118,10 @@ struct Cfg {
   static constexpr int kMrgHalf = (LC / 2) * kMaxHeads * 4;               // merge: one half partial slice
   static constexpr int kStgBytes = kMaxHeads * (LC * 2 + 16);             // merge: staged output rows
   static constexpr int kSmem = 1024 + kRegionBytes + (int)sizeof(Smem);
-  static_assert(LC % 64 == 0 && (CL == 1 || CL == 2), "latent slice");
+  static_assert(LC % 64 == 0 && (CL == 1 || CL == 2 || CL == 4), "latent slice");
   static_assert(kQCol + QT / 2 <= 512, "TMEM columns");
   static_assert(kStgBytes + 2 * kMrgHalf <= kRegionBytes, "merge buffers in the idle region");
-  static_assert(NRH % CL == 0, "raw boxes split over the cluster");
+  static_assert(kMode != kLoadFp8 || NRH % CL == 0, "raw boxes split over the cluster");
   static_assert(QT / 64 <= NQS + 1, "the query staging fits the query buffer");
   static_assert(kSmem <= 232448, "shared memory");
 };
@@ -240,9 +245,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 // Partials of split tokens are stored interleaved, [partition, slot, L / 4, H]
 // float4: a warp's 32 head rows of one 4-column chunk are 512 contiguous bytes,
-// and one CTA's latent half of one partial is a single contiguous block.
-__device__ __forceinline__ size_t part_index(int k, int slot, int c, int row, int L, int H) {
-  return ((size_t)(k * 2 + slot) * (L / 4) + c) * H + row;
+// and one CTA's latent half of one partial is a single contiguous block.  A
+// partition has 2 * ns slots: its first and its last segment, each with ns token
+// slots (two when tokens are folded in pairs); slot = segment slot * ns + token slot.
+__device__ __forceinline__ size_t part_index(int k, int slot, int c, int row, int L, int H, int ns) {
+  return ((size_t)(k * 2 * ns + slot) * (L / 4) + c) * H + row;
 }
 
 // Log-sum-exp merge of one split token's partials for head `row`, latent
@@ -254,12 +261,13 @@ __device__ __forceinline__ size_t part_index(int k, int slot, int c, int row, in
 // (the merging CTA's own partial still in TMEM, its stage ring idle) runs in
 // the softmax epilogue instead.
 __device__ __noinline__ void merge_split_token(const DecodeArgs& a, int t, const TokenPlan& tp, int kf, int kl,
-                                               int slot_kf, uint32_t rank, int row, int lat_x0, int LC) {
+                                               int slot_kf, uint32_t rank, int row, int lat_x0, int LC, int ns,
+                                               int ts) {
   const int H = a.d.num_heads, L = a.d.kv_lora_rank;
   const float4* __restrict__ part_o = reinterpret_cast<const float4*>(a.part_o);
   const float* __restrict__ part_lse = a.part_lse;
-  auto slot_of = [&](int k) { return k == kf ? slot_kf : 0; };
-  auto lse_of = [&](int k) { return __ldcg(part_lse + ((size_t)(k * 2 + slot_of(k)) * 2 + rank) * H + row); };
+  auto slot_of = [&](int k) { return (k == kf ? slot_kf : 0) * ns + ts; };
+  auto lse_of = [&](int k) { return __ldcg(part_lse + ((size_t)(k * 2 * ns + slot_of(k)) * 2 + rank) * H + row); };
   float mx = -CUDART_INF_F;
   for (int k = kf; k <= kl; ++k) mx = fmaxf(mx, lse_of(k));
   float sum = 0.f;
@@ -276,7 +284,7 @@ __device__ __noinline__ void merge_split_token(const DecodeArgs& a, int t, const
         const int c0 = (lat_x0 + col0) / 4;
         float4 u[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) u[i] = __ldcg(part_o + part_index(k, slot_of(k), c0 + i, row, L, H));
+        for (int i = 0; i < 8; ++i) u[i] = __ldcg(part_o + part_index(k, slot_of(k), c0 + i, row, L, H, ns));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           acc[i].x = fmaf(w, u[i].x, acc[i].x);
@@ -323,15 +331,15 @@ template <int LC>
 __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t, const TokenPlan& tp, int k, int kf,
                                            int kl, int slot_kf, uint32_t rank, int row, int lat_x0, uint32_t trow,
                                            uint32_t tacc, float lse_own, float inv, uint8_t* stg, uint8_t* hb,
-                                           int& nmrg) {
+                                           int& nmrg, int ns, int ts) {
   constexpr int LH = LC / 2;                            // columns per half slice
   constexpr uint32_t kHalf = (uint32_t)LH * kMaxHeads * 4;
   constexpr int kStgStride = LC * 2 + 16;               // bytes per staged row
   const int H = a.d.num_heads, L = a.d.kv_lora_rank;
   PlanHeader* hdr = a.hdr_mut;
   const bool live = row < H;
-  auto slot_of = [&](int kk) { return kk == kf ? slot_kf : 0; };
-  auto lse_ptr = [&](int kk) { return a.part_lse + ((size_t)(kk * 2 + slot_of(kk)) * 2 + rank) * H + row; };
+  auto slot_of = [&](int kk) { return (kk == kf ? slot_kf : 0) * ns + ts; };
+  auto lse_ptr = [&](int kk) { return a.part_lse + ((size_t)(kk * 2 * ns + slot_of(kk)) * 2 + rank) * H + row; };
   const int np = kl - kf + 1;
   const int nj = 2 * (np - 1);                          // half slices to bring in
   const uint32_t half_bytes = (uint32_t)(LH * H * 4);
@@ -342,7 +350,8 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
     if (p >= k) ++p;
     mbar_arrive_expect_tx(&cs->mrg_full[b], half_bytes);
     bulk_copy_g2s(hb + b * kHalf,
-                  reinterpret_cast<const float4*>(a.part_o) + part_index(p, slot_of(p), lat_x0 / 4 + (j & 1) * (LH / 4), 0, L, H),
+                  reinterpret_cast<const float4*>(a.part_o) +
+                      part_index(p, slot_of(p), lat_x0 / 4 + (j & 1) * (LH / 4), 0, L, H, ns),
                   half_bytes, &cs->mrg_full[b]);
     return true;
   };
@@ -475,8 +484,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   Smem* cs = reinterpret_cast<Smem*>(sStage + S * C::kStageBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t rank = CL == 2 ? cluster_ctarank() : 0u;
-  const uint32_t peer = rank ^ 1u;
+  const uint32_t crank = CL >= 2 ? cluster_ctarank() : 0u;   // rank in the cluster
+  const uint32_t rank = crank % C::NHALF;                      // latent half of O this CTA owns
+  const int tslot = (int)(crank / C::NHALF);                   // query token slot (folded pairs)
   const int k = blockIdx.x / CL;
   PlanHeader* hdr = a.hdr_mut;
   const int H = a.d.num_heads;
@@ -508,7 +518,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       mbar_init(&cs->mrg_full[i], 1);
       mbar_init(&cs->mrg_done[i], 128);
     }
-    mbar_init(&cs->bye, 1);
+    mbar_init(&cs->bye, CL > 1 ? CL - 1 : 1);   // one arrival from every other CTA
     cs->abort = 0;
     fence_mbar_init();
   }
@@ -523,7 +533,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   }
   tc_fence_before();
   // both CTAs' barriers are initialised before either multicasts into the other
-  if (CL == 2) cluster_sync(); else __syncthreads();
+  if (CL >= 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = cs->tmem_base;
   // the W_uv kernel may start its prologue now; the plan and q_full of the
@@ -538,12 +548,13 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     auto load_box = [&](void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-      if (CL == 2) tma_load_2d_mc(dst, map, bar, x, y, (uint16_t)0x3);
+      if (CL >= 2) tma_load_2d_mc(dst, map, bar, x, y, (uint16_t)C::kMcMask);
       else tma_load_2d(dst, map, bar, x, y);
     };
     int c = 0;
     bool bad = false;
     for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int next_t) {
+      const int tq = tslot < tp.ntok ? t + tslot : t;   // this CTA's query token (slot 0's when none)
       bool q_pending = true;   // the query's shared-memory part goes right after the first tile
       // The next segment's absorbed query is read at this segment's end; it goes
       // into L2 a few tiles before that (earlier, the cache stream evicts it again).
@@ -616,9 +627,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           if (!pm) continue;
           const int y = load_row(it, p, pm, pg);
           if (lane < kOwn) {
-            if (MODE == kLoadFp8) tma_prefetch_2d(&maps.kv_lat, ((int)rank * kOwn + lane) * C::RW, y);
-            else tma_prefetch_2d(&maps.kv_lat, 64 * ((int)rank * kOwn + lane), y);
-          } else if (lane == kOwn && rank == 0) {
+            if (MODE == kLoadFp8) tma_prefetch_2d(&maps.kv_lat, ((int)crank * kOwn + lane) * C::RW, y);
+            else tma_prefetch_2d(&maps.kv_lat, 64 * ((int)crank * kOwn + lane), y);
+          } else if (lane == kOwn && crank == 0) {
             tma_prefetch_2d(&maps.kv_rope, rope_x0, y);
           }
         }
@@ -627,7 +638,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (lane == 0) {
           mbar_arrive_expect_tx(&cs->qa_full, (C::QT / 64) * C::kQBox);
           for (int i = 0; i < C::QT / 64; ++i)
-            tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->qa_full, 64 * i, t * kMaxHeads);
+            tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->qa_full, 64 * i, tq * kMaxHeads);
         }
         __syncwarp();
       };
@@ -646,8 +657,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       for (int it = ia; it < ie; ++it, ++c) {
         if (waborted(cs)) return;
         const int s = c % S;
-        if (lane == 0 && it == q_prefetch_at && next_t >= 0 && next_t < a.T)
-          bulk_prefetch_l2(a.q_full + (size_t)next_t * kMaxHeads * KQ, (uint32_t)(kMaxHeads * KQ * 2));
+        if (lane == 0 && it == q_prefetch_at && next_t >= 0 && next_t + tslot < a.T)
+          bulk_prefetch_l2(a.q_full + (size_t)(next_t + tslot) * kMaxHeads * KQ, (uint32_t)(kMaxHeads * KQ * 2));
         if (it == q_prefetch_at && next_t < 0 && ie < tp.ntiles) {
           // the partition's last segment ends inside its token: if this partition
           // finishes the token last it merges the later partitions' partials
@@ -655,10 +666,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           // of them into L2 now (one lane per partition)
           const int kl = tp.part_last;
           const int L4 = L / 4, Hh = a.d.num_heads;
+          constexpr int NS = C::NSLOT;
           for (int kk = k + 1 + lane; kk <= kl; kk += 32) {
-            bulk_prefetch_l2(reinterpret_cast<const float4*>(a.part_o) + ((size_t)(kk * 2) * L4 + lat_x0 / 4) * Hh,
+            bulk_prefetch_l2(reinterpret_cast<const float4*>(a.part_o) + ((size_t)(kk * 2 * NS + tslot) * L4 + lat_x0 / 4) * Hh,
                              (uint32_t)(LC * Hh * 4));
-            bulk_prefetch_l2(a.part_lse + (size_t)(kk * 2) * 2 * Hh, (uint32_t)(2 * Hh * 4));
+            bulk_prefetch_l2(a.part_lse + (size_t)(kk * 2 * NS + tslot) * 2 * Hh, (uint32_t)(2 * Hh * 4));
           }
         }
         // global reads of this tile and (bf16 pool) of the one two ahead, for its
@@ -700,24 +712,24 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             constexpr int kOwnBoxes = C::NLB / CL;
 #pragma unroll
             for (int j = 0; j < kOwnBoxes; ++j) {
-              const int i = (int)rank * kOwnBoxes + j;
-              if (CL == 2)
+              const int i = (int)crank * kOwnBoxes + j;
+              if (CL >= 2)
                 tma_gather4_mc(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y0, y1, y2, y3,
-                               (uint16_t)0x3);
+                               (uint16_t)C::kMcMask);
               else
                 tma_gather4(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y0, y1, y2, y3);
             }
-            if (rank == 0) {
-              if (CL == 2)
+            if (crank == 0) {
+              if (CL >= 2)
                 tma_gather4_mc(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y0, y1, y2, y3,
-                               (uint16_t)0x3);
+                               (uint16_t)C::kMcMask);
               else
                 tma_gather4(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y0, y1, y2, y3);
             }
           }
         } else {
           // pages of this tile that hold at least one live row; both CTAs count the
-          // same bytes, half of which the peer's multicast delivers
+          // same bytes, most of which the other CTAs' multicasts deliver
           const uint32_t row_bytes = (MODE == kLoadFp8 ? L : C::NLB * 128) + 128;
           uint32_t live_rows = 0;
           for (int p = 0; p < nloads; ++p)
@@ -735,13 +747,13 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             // one box per lane: this CTA's share of the latent (or raw e4m3) boxes, then the rope box (rank 0)
             if (lane < kOwn) {
               if (MODE == kLoadFp8) {
-                const int h = (int)rank * kOwn + lane;
+                const int h = (int)crank * kOwn + lane;
                 load_box(st + C::kRawOff + h * 64 * C::RW + r0 * C::RW, &maps.kv_lat, &cs->kv_full[s], h * C::RW, y);
               } else {
-                const int i = (int)rank * kOwn + lane;
+                const int i = (int)crank * kOwn + lane;
                 load_box(st + i * C::kBox + r0 * 128, &maps.kv_lat, &cs->kv_full[s], 64 * i, y);
               }
-            } else if (lane == kOwn && rank == 0) {
+            } else if (lane == kOwn && crank == 0) {
               load_box(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y);
             }
           }
@@ -766,8 +778,8 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           if (lane == 0) {
             mbar_arrive_expect_tx(&cs->q_full, C::kQBytes);
             for (int i = 0; i < C::NQS; ++i)
-              tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->q_full, C::QT + 64 * i, t * kMaxHeads);
-            tma_load_2d(sQ + C::NQS * C::kQBox, &maps.q, &cs->q_full, L, t * kMaxHeads);
+              tma_load_2d(sQ + i * C::kQBox, &maps.q, &cs->q_full, C::QT + 64 * i, tq * kMaxHeads);
+            tma_load_2d(sQ + C::NQS * C::kQBox, &maps.q, &cs->q_full, L, tq * kMaxHeads);
           }
           __syncwarp();
           q_pending = false;
@@ -781,7 +793,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       for (int j = c - S; j < c; ++j) {
         if (j < 0) continue;
         mbar_wait(&cs->kv_full[j % S], (j / S) & 1, kWaitLimitNs);
-        if (CL == 2) mbar_wait(&cs->kv_empty[j % S], (j / S) & 1, kWaitLimitNs);
+        if (CL >= 2) mbar_wait(&cs->kv_empty[j % S], (j / S) & 1, kWaitLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -892,7 +904,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(tmem, tmem + C::kSCol + 64 * b + 8 * kk, dv + (uint64_t)((kk * 2048) >> 4), idesc_pv,
                    (it == ia && kk == 0) ? 0u : 1u);
-          if (CL == 2) mma_commit_mc(&cs->kv_empty[cp % S], (uint16_t)0x3);
+          if (CL >= 2) mma_commit_mc(&cs->kv_empty[cp % S], (uint16_t)C::kMcMask);
           else mma_commit(&cs->kv_empty[cp % S]);
           mma_commit(&cs->pv_done[b]);
         }
@@ -984,9 +996,20 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     TokenPlan pend_tp{};
     int nmrg = 0;   // half partials brought in by bulk copy (buffer and phase of mrg_full / mrg_done)
     bool q_ready = false;   // the coming segment's query is already in TMEM
-    for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
+    for_each_segment(a, k, g0, g1, [&](int si, int t0, const TokenPlan& tp, int ia, int ie, bool is_first_seg,
                                      int next_t) {
       if (waborted(cs)) return;
+      // this CTA's query token: slot tslot of a folded pair; a slot the pair does
+      // not fill repeats slot 0's work without writing anything
+      const bool shadow = C::NSLOT > 1 && tslot >= (tp.ntok > 1 ? tp.ntok : 1);
+      const int t = shadow ? t0 : t0 + tslot;
+      int mlo = tp.lo, mhi = tp.hi;
+      if constexpr (C::NSLOT > 1) {
+        mlo = tslot == 0 ? tp.mlo : a.plan[t].mlo;
+        mhi = tslot == 0 ? tp.mhi : a.plan[t].mhi;
+      }
+      // a folded token may attend fewer keys than the tiles of its pair cover
+      const bool own_mask = C::NSLOT > 1 && (mlo > tp.lo || mhi < tp.hi);
       if (!q_ready && !copy_q(si)) return;
       q_ready = false;
       float m = -CUDART_INF_F, l = 0.f;
@@ -995,7 +1018,15 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (waborted(cs)) return;
         const int s = c % S, b = c & 1;
         if (!wwait(&cs->kv_full[s], (c / S) & 1, cs, hdr)) return;   // row mask visibility
-        const uint64_t mask = cs->row_mask[s];
+        uint64_t mask = cs->row_mask[s];
+        if (own_mask) {
+          // keys of the tile outside this token's own range do not count
+          const int key0 = (tp.tile_first + it) * kTileKeys;
+          const int a0 = mlo - key0, a1 = mhi - key0;
+          const uint64_t above = a0 <= 0 ? ~0ull : (a0 >= 64 ? 0ull : ~0ull << a0);
+          const uint64_t below = a1 >= 64 ? ~0ull : (a1 <= 0 ? 0ull : (1ull << a1) - 1);
+          mask &= above & below;
+        }
         if (!wwait(&cs->s_full[b], (c >> 1) & 1, cs, hdr)) return;
         tc_fence_after();
         // S row (64 fp32) for this thread's head; both halves of the load in flight at once
@@ -1105,6 +1136,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       }
       const bool complete = ia == 0 && ie == tp.ntiles;
       const bool final_seg = tp.tile_start + ie >= g1;   // the partition's last segment
+      constexpr int NS = C::NSLOT;
       const int kf = tp.part_first, kl = tp.part_last;
       // partition kf holds the token in its second slot if the token began inside its range
       const int slot_kf = complete ? 0 : (tp.tile_start != a.bounds[kf] ? 1 : 0);
@@ -1117,7 +1149,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       // outcome; it is decided after the partition's final segment.  A claimer
       // that does not merge depends on nothing outside its CTA from its claim to
       // its written count, so a merger's wait ends.
-      const bool early_claim = !complete && final_seg;
+      const bool early_claim = !complete && final_seg && !shadow;
       int claim = 0;
       if (early_claim && row == 0) claim = atomicAdd(&a.counters[4 * t + rank], 1);
       if (!wwait(&cs->pv_done[last_c & 1], (last_c >> 1) & 1, cs, hdr)) return;
@@ -1143,10 +1175,10 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         ++nfix;
         merger = cs->fix_last;
       }
-      const int slot = is_first_seg ? 0 : 1;
+      const int slot = (is_first_seg ? 0 : 1) * NS + tslot;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
-      const bool live = row < H;
+      const bool live = row < H && !shadow;
       if (!merger) {
 #pragma unroll 1
         for (int col = 0; col < LC; col += 32) {
@@ -1166,7 +1198,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             float4* po = reinterpret_cast<float4*>(a.part_o);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              po[part_index(k, slot, (lat_x0 + col) / 4 + i, row, L, H)] =
+              po[part_index(k, slot, (lat_x0 + col) / 4 + i, row, L, H, NS)] =
                   make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
                               __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
           }
@@ -1175,19 +1207,19 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           if (complete) {
             if (rank == 0) a.lse_ws[(size_t)t * H + row] = lse;
           } else {
-            a.part_lse[((size_t)(k * 2 + slot) * 2 + rank) * H + row] = lse;
+            a.part_lse[((size_t)(k * 2 * NS + slot) * 2 + rank) * H + row] = lse;
           }
         }
       }
       // O has been read: the next segment's first P . C may overwrite it
       tc_fence_before();
       mbar_arrive(&cs->o_free);
-      if (complete) return;
+      if (complete || shadow) return;
       if (merger) {
         // the partition's final segment: O in TMEM still holds this CTA's own
         // partial and the query buffer and stage ring are idle
         if (!merge_in_tmem<LC>(a, cs, t, tp, k, kf, kl, slot_kf, rank, row, lat_x0, trow, trow + C::kSCol, lse, inv, sQ,
-                               sQ + C::kRegionBytes - 2 * C::kMrgHalf, nmrg))
+                               sQ + C::kRegionBytes - 2 * C::kMrgHalf, nmrg, NS, tslot))
           return;
         if (row == 0) {
           a.counters[4 * t + rank] = 0;
@@ -1233,7 +1265,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         mbar_arrive(&cs->fix_done);
       }
       if (wwait(&cs->fix_done, nfix & 1, cs, hdr) && !waborted(cs) && cs->fix_last) {
-        if (row < H) merge_split_token(a, pend_t, pend_tp, kf, kl, slot_kf, rank, row, lat_x0, LC);
+        if (row < H) merge_split_token(a, pend_t, pend_tp, kf, kl, slot_kf, rank, row, lat_x0, LC, C::NSLOT, tslot);
         if (row == 0) {
           a.counters[4 * pend_t + rank] = 0;
           a.counters[4 * pend_t + 2 + rank] = 0;
@@ -1245,13 +1277,14 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
   // ------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (CL == 2 && tid == 32) {
-    // Tell the peer this CTA is done, and wait (bounded) until the peer says the
-    // same before this CTA's shared memory goes away.  Everything the peer sends
+  if (CL >= 2 && tid == 32) {
+    // Tell the other CTAs this CTA is done, and wait (bounded) until they have all
+    // said the same before this CTA's shared memory goes away.  Everything they send
     // into this CTA (multicast tiles, multicast stage commits) has been awaited on
     // this CTA's own barriers already, so the signal needs no release ordering (a
     // release at cluster scope here stalled for tens of microseconds).
-    mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&cs->bye), peer));
+    for (uint32_t r = 0; r < (uint32_t)CL; ++r)
+      if (r != crank) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&cs->bye), r));
     if (!mbar_poll_cluster(&cs->bye, 0, kWaitLimitNs)) {
       record_timeout(&cs->bye, hdr);
       atomicOr(&hdr->status, kDeviceTimeout);
@@ -1419,9 +1452,48 @@ cudaError_t launch(const DecodeArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, decode_tc_kernel<LC, CL, MODE>, maps, a);
 }
 
+// Clusters of this instance that the device holds at once (its shared memory, its
+// cluster size): the default partition count, so that no partition waits for a
+// second wave.  Cached per device.
+template <int LC, int CL, int MODE>
+int max_active_clusters() {
+  using C = Cfg<LC, CL, MODE>;
+  static std::mutex mu;
+  static int cached[64] = {};
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[device] > 0) return cached[device];
+  if (ensure_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<LC, CL, MODE>), C::kSmem) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * 256);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<LC, CL, MODE>, &cfg) != cudaSuccess) {
+    cudaGetLastError();   // a failed query leaves no error behind
+    return 0;
+  }
+  cached[device] = n;
+  return n;
+}
+
 template <int MODE>
 cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t s) {
-  if (a.d.kv_lora_rank == 512) return launch<256, 2, MODE>(a, s);
+  if (a.d.kv_lora_rank == 512) {
+    if constexpr (MODE != kLoadFp8) {
+      if (a.fold) return launch<256, 4, MODE>(a, s);
+    }
+    return launch<256, 2, MODE>(a, s);
+  }
   return launch<64, 1, MODE>(a, s);
 }
 
@@ -1430,6 +1502,25 @@ cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t s) {
 // Shapes with a tensor-core instance: (L, R) = (512, 64) on a 2-CTA cluster,
 // and L = 64 with R <= 32 on one CTA; qk_nope and v_head multiples of 8, v_head <= 512;
 // dense pages of 8..64 tokens or a multiple of 64.
+int decode_default_partitions(const mla_dims_t& d, bool fold, bool fp8_cache, bool sparse) {
+  if (d.kv_lora_rank != 512) {
+    if (sparse) return tc::max_active_clusters<64, 1, tc::kLoadSparse>();
+    if (fp8_cache) return tc::max_active_clusters<64, 1, tc::kLoadFp8>();
+    return tc::max_active_clusters<64, 1, tc::kLoadDense>();
+  }
+  if (fold && !fp8_cache) {
+    if (sparse) return tc::max_active_clusters<256, 4, tc::kLoadSparse>();
+    return tc::max_active_clusters<256, 4, tc::kLoadDense>();
+  }
+  if (sparse) return tc::max_active_clusters<256, 2, tc::kLoadSparse>();
+  if (fp8_cache) return tc::max_active_clusters<256, 2, tc::kLoadFp8>();
+  return tc::max_active_clusters<256, 2, tc::kLoadDense>();
+}
+
+bool decode_fold_supported(const mla_dims_t& d, bool fp8_cache) {
+  return d.kv_lora_rank == 512 && d.qk_rope == 64 && !fp8_cache;
+}
+
 bool decode_tc_supported(const mla_dims_t& d) {
   const int ps = d.page_size;
   // the weight GEMMs read q and w_uk rows through TMA (16-byte row pitch),

@@ -27,6 +27,7 @@ struct DecodeArgs {
   float* part_lse;              // [K, 2, 2, H]
   int* counters;                // [T, 4]
   const int* bounds;            // [2K + 1] first global tile of each partition, the total, first tokens
+  bool fold;                    // query tokens walked in pairs by clusters of four CTAs
 };
 
 
@@ -38,6 +39,10 @@ cudaError_t ensure_smem_limit(const void* func, int bytes);
 
 // Tensor-core decode (tcgen05): dense bf16 paged cache, shapes listed in decode_tc_supported.
 bool decode_tc_supported(const mla_dims_t& d);
+// Shapes with a folded (pairs of query tokens, cluster of four) decode instance.
+bool decode_fold_supported(const mla_dims_t& d, bool fp8_cache);
+// Partitions the device runs at once for this instance (0 if the query failed).
+int decode_default_partitions(const mla_dims_t& d, bool fold, bool fp8_cache, bool sparse);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t s);
 
 // One thread waits (bounded by limit_ns) on an mbarrier nothing arrives on and

@@ -23,7 +23,15 @@ struct PlanInputs {
   __nv_bfloat16* o_lat;      // [T, H, L]: zeroed for tokens without keys
   float* lse_ws;             // [T, H]:    -inf for tokens without keys
   int H, L;
+  bool fold;                 // pair consecutive tokens of a request (they share tiles)
 };
+
+// Key range [lo, hi) of the query at position pos of request b with cache_len len.
+__device__ __forceinline__ void plan_key_range(int mask, int window, int len, int pos, int& lo, int& hi) {
+  if (mask == MLA_MASK_NULL) { lo = 0; hi = len; }
+  else if (mask == MLA_MASK_CAUSAL) { lo = 0; hi = pos + 1; }
+  else { hi = pos + 1; lo = max(0, hi - window); }
+}
 
 // Whole block (blockDim.x a multiple of 32, <= 1024).  Each thread owns a
 // contiguous run of tokens and counts their tiles; a block-wide exclusive scan
@@ -58,26 +66,46 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
     }
     const int qb = (int)in.offsets[b], qe = (int)in.offsets[b + 1];
     int lo = 0, hi = 0;
+    int ulo = 0, uhi = 0;   // the tiles walked: the token's own range, or its pair's union
+    int ntok = 1;
     bool ok = qb <= t && t < qe && (int)in.offsets[in.B] == in.T;
+    const bool follower = in.fold && ((t - qb) & 1);
+    const bool paired = in.fold && !follower && t + 1 < qe;
     if (ks.indices) {
       int cnt = ks.topk_lengths ? ks.topk_lengths[b] : ks.idx_stride;
       if (cnt < 0) { cnt = 0; ok = false; }
       hi = min(cnt, ks.idx_stride);
+      ulo = lo;
+      uhi = hi;                          // a request's tokens share its index list
     } else {
       const int len = (int)ks.cache_lens[b];
       const int pos = len - (qe - qb) + (t - qb);
       if (len > ks.bt_stride * ks.page_size || pos < 0) ok = false;
-      if (in.mask == MLA_MASK_NULL) { lo = 0; hi = len; }
-      else if (in.mask == MLA_MASK_CAUSAL) { lo = 0; hi = pos + 1; }
-      else { hi = pos + 1; lo = max(0, hi - in.window); }
+      plan_key_range(in.mask, in.window, len, pos, lo, hi);
+      ulo = lo;
+      uhi = hi;
+      if (paired) {
+        int lo2, hi2;
+        plan_key_range(in.mask, in.window, len, pos + 1, lo2, hi2);
+        if (hi2 > lo2) {
+          if (uhi > ulo) { ulo = min(ulo, lo2); uhi = max(uhi, hi2); }
+          else { ulo = lo2; uhi = hi2; }
+        }
+      }
     }
-    if (!ok) { lo = 0; hi = 0; bad = true; }
+    if (!ok) { lo = hi = ulo = uhi = 0; bad = true; }
+    if (paired) ntok = 2;
+    if (follower) { ulo = uhi = 0; ntok = 0; }
     TokenPlan p;
     p.b = b;
-    p.lo = lo;
-    p.hi = hi;
-    p.tile_first = hi > lo ? lo / kTileKeys : 0;
-    p.ntiles = hi > lo ? (hi + kTileKeys - 1) / kTileKeys - p.tile_first : 0;
+    p.lo = ulo;
+    p.hi = uhi;
+    p.mlo = lo;
+    p.mhi = hi;
+    p.ntok = ntok;
+    p.pad = 0;
+    p.tile_first = uhi > ulo ? ulo / kTileKeys : 0;
+    p.ntiles = uhi > ulo ? (uhi + kTileKeys - 1) / kTileKeys - p.tile_first : 0;
     p.tile_start = my_tiles;   // local for now
     p.part_first = p.part_last = 0;
     in.plan[t] = p;
@@ -192,9 +220,12 @@ __device__ __forceinline__ void plan_block(const PlanInputs& in) {
   if (tid == 0) in.bounds[K] = total;
   __syncthreads();
   // tokens with no key: zero latent output and lse = -inf (the decode never visits
-  // them); each thread clears its own tokens
+  // them); each thread clears its own tokens.  A pair's second token is written by
+  // the decode unless the pair walks no tile.
   for (int t = t0; t < t1; ++t) {
-    if (in.plan[t].ntiles != 0) continue;
+    const TokenPlan& p = in.plan[t];
+    if (p.ntiles != 0) continue;
+    if (p.ntok == 0 && t > 0 && in.plan[t - 1].ntiles != 0 && in.plan[t - 1].ntok == 2) continue;
     uint4* o = reinterpret_cast<uint4*>(in.o_lat + (size_t)t * in.H * in.L);
     for (int i = 0; i < in.H * in.L / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
     for (int i = 0; i < in.H; ++i) in.lse_ws[(size_t)t * in.H + i] = -CUDART_INF_F;

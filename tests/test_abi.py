@@ -92,7 +92,8 @@ def test_invalid_arguments_are_rejected(lib):
     assert _paged(lib, opts=_opts(mask=2, window=0)) == 1             # SWC needs window >= 1
     assert _paged(lib, opts=_opts(scale=float("nan"))) == 1
     assert _paged(lib, opts=_opts(num_splits=-1)) == 1
-    assert _paged(lib, opts=_opts(flags=8)) == 1
+    assert _paged(lib, opts=_opts(flags=16)) == 1                     # unknown flag
+    assert _paged(lib, opts=_opts(flags=4 | 8)) == 1                  # both query walks forced
 
 
 def test_unsupported_shapes_are_reported(lib):
@@ -119,15 +120,16 @@ def test_fp8_q_scale_and_sparse_mask_are_unsupported(lib):
     assert rc == 2
 
 
-def _expected_workspace(H, L, R, T, K):
+def _expected_workspace(H, L, R, T, K, NI=1):
     """The workspace sections in order, each starting on a 256-byte boundary:
-    plan header, TokenPlan[T] (32 bytes), counters int[T, 4], bounds int[2K + 1],
+    plan header, TokenPlan[T] (48 bytes), counters int[T, 4], bounds int[2K + 1],
     q_full bf16 [T, 128, L + R], o_lat bf16 [T, H, L], lse f32 [T, H],
-    partials f32 [K, 2, H, L] and their lse f32 [K, 2, 2, H]."""
+    partials f32 [K, 2 NI, H, L] and their lse f32 [K, 2 NI, 2, H] (NI = 2 token slots
+    when tokens are walked in pairs)."""
     up = lambda x: (x + 255) & ~255
     o = up(256)
-    for size in (32 * max(T, 1), 16 * max(T, 1), 4 * (2 * K + 1), T * 128 * (L + R) * 2,
-                 T * H * L * 2, T * H * 4, K * 2 * H * L * 4, K * 2 * 2 * H * 4):
+    for size in (48 * max(T, 1), 16 * max(T, 1), 4 * (2 * K + 1), T * 128 * (L + R) * 2,
+                 T * H * L * 2, T * H * 4, K * 2 * NI * H * L * 4, K * 2 * NI * 2 * H * 4):
         o = up(o + size)
     return o
 
@@ -142,3 +144,15 @@ def test_workspace_size_matches_the_section_layout(lib, H, L, R, T, K):
     assert lib.mla_decode_workspace_size(ctypes.byref(dims), ctypes.byref(_opts(num_splits=K)), max(T, 1), T,
                                          ctypes.byref(n)) == 0
     assert n.value == _expected_workspace(H, L, R, T, K)
+
+
+@pytest.mark.parametrize("T,B,K", [(64, 32, 38), (6, 3, 5), (64, 64, 38)])
+def test_workspace_size_covers_folded_pairs(lib, T, B, K):
+    # two or more tokens per request: partials get two token slots; the size returned
+    # covers both walks (folded and one token at a time) for the same split count
+    n = ctypes.c_size_t()
+    assert lib.mla_decode_workspace_size(ctypes.byref(_dims()), ctypes.byref(_opts(num_splits=K)), B, T,
+                                         ctypes.byref(n)) == 0
+    fold = T >= 2 * B
+    want = max(_expected_workspace(128, 512, 64, T, K, 2 if fold else 1), _expected_workspace(128, 512, 64, T, K))
+    assert n.value == want

@@ -59,15 +59,19 @@ def compare(p, out_gpu, lse_gpu, out_ref, lse_ref, tokens=None):
 
 def split_tokens(ws, T):
     """Query tokens the call's plan cut between KV partitions (read back from the workspace:
-    TokenPlan[T] of 8 int32 at byte 256; fields 6 and 7 are its first and last partition)."""
-    plan = ws[256:256 + 32 * T].cpu().numpy().view(np.int32).reshape(T, 8)
-    return [int(t) for t in np.flatnonzero(plan[:, 6] != plan[:, 7])]
+    TokenPlan[T] of 12 int32 at byte 256; fields 6 and 7 are its first and last partition,
+    field 10 the tokens walked with its tiles: 2 for the first of a folded pair)."""
+    plan = ws[256:256 + 48 * T].cpu().numpy().view(np.int32).reshape(T, 12)
+    cut = np.flatnonzero((plan[:, 6] != plan[:, 7]) & (plan[:, 5] > 0))
+    out = set(int(t) for t in cut)
+    out |= set(int(t) + 1 for t in cut if plan[t, 10] == 2)      # the pair's second token
+    return sorted(out)
 
 
-def check(p, dev, num_splits=0, tokens=None, with_split_tokens=True):
+def check(p, dev, num_splits=0, tokens=None, with_split_tokens=True, fold_pairs=None):
     d = device_inputs(p, dev)
     ws = torch.empty(max(256, workspace_bytes(p, num_splits)), dtype=torch.uint8, device=dev)
-    out, lse = run_gpu(p, d, num_splits=num_splits, debug=True, workspace=ws)
+    out, lse = run_gpu(p, d, num_splits=num_splits, debug=True, workspace=ws, fold_pairs=fold_pairs)
     torch.cuda.synchronize()
     if tokens is not None and with_split_tokens:
         tokens = sorted(set(tokens) | set(split_tokens(ws, p.T)))
@@ -255,6 +259,97 @@ def test_bad_page_id_is_reported_not_dereferenced(dev):
     assert ei.value.code == 5
 
 
+# ------------------------------------------------------------------ folded token pairs
+# Requests with several query tokens: consecutive tokens walk their cache tiles in pairs
+# (one tile load for both) when MLA_FLAG_FOLD_PAIRS asks for it, and by default in sparse calls.
+
+@pytest.mark.parametrize("num_splits", [0, 1, 3, 40])
+def test_folded_pairs(dev, num_splits):
+    # (with only two keys a token's latent output is an average of two rows, and its bf16
+    # rounding alone moves single outputs by up to ~2e-2: the shortest cache here gives
+    # the first token of its pair six keys)
+    p = dsv3_small(lens=(7, 70, 300, 1000, 129), qlens=(2, 2, 2, 2, 2), num_pages=64)
+    check(p, dev, num_splits=num_splits, fold_pairs=True)
+
+
+@pytest.mark.parametrize("qlens", [(1, 2, 3, 4), (3, 1, 1, 5)])
+def test_folded_ragged_query_counts(dev, qlens):
+    # odd counts leave a pair's second slot empty; single-token requests too
+    check(dsv3_small(lens=(10, 200, 650, 131), qlens=qlens, num_pages=64), dev, fold_pairs=True)
+
+
+@pytest.mark.parametrize("mask,window", [(W.MASK_NULL, 0), (W.MASK_SLIDING_WINDOW_CAUSAL, 1),
+                                         (W.MASK_SLIDING_WINDOW_CAUSAL, 100)])
+def test_folded_masks(dev, mask, window):
+    check(dsv3_small(lens=(8, 130, 700, 64), qlens=(2, 2, 2, 2), mask=mask, window=window), dev,
+          num_splits=3, fold_pairs=True)
+
+
+def test_folded_agrees_with_one_token_at_a_time(dev):
+    p = dsv3_small(lens=(3000, 64, 2500, 640, 1), qlens=(2, 2, 2, 2, 1), num_pages=160)
+    d = device_inputs(p, dev)
+    a, la = run_gpu(p, d, debug=True, fold_pairs=True)
+    b, lb = run_gpu(p, d, debug=True, fold_pairs=False)
+    torch.cuda.synchronize()
+    x, y = a.float(), b.float()
+    assert torch.isfinite(x).all()
+    assert (torch.linalg.norm(x - y) / torch.linalg.norm(y)).item() <= TOL_BF16_REL_L2
+    assert (la - lb).abs().max().item() <= 1e-3
+
+
+def test_default_walk_dense_one_token_sparse_pairs(dev):
+    """With two tokens per request a dense call walks one token at a time and a sparse
+    call folds pairs unless told otherwise: the default's bits equal the forced walk's."""
+    p = dsv3_small(lens=(300, 64, 1000), qlens=(2, 2, 2), num_pages=32)
+    s = _sparse_pairs("sparse_default_walk", 36, topk=[512, 77, 1024], stride=1024)
+    for prob, walk in ((p, False), (s, True)):
+        d = device_inputs(prob, dev)
+        a, la = run_gpu(prob, d, debug=True)
+        b, lb = run_gpu(prob, d, debug=True, fold_pairs=walk)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b) and torch.equal(la, lb)
+
+
+def _sparse_pairs(name, seed, topk, stride, tokens_per_request=4096):
+    """A sparse problem with two query tokens per request (they share its index list)."""
+    s = W.make_sparse(name, seed, **DSV3, ps=64, tokens_per_request=tokens_per_request,
+                      topk_lengths=topk, stride=stride, inner_pad_frac=0.05)
+    B = s.B
+    q = W.to_bf16_bits(W.Stream(seed, name + "-q2").normal(2 * B * s.H * (s.N + s.R)).reshape(2 * B, s.H, s.N + s.R))
+    return dataclasses.replace(s, T=2 * B, q=q, row_offsets=(2 * np.arange(B + 1)).astype(np.uint32))
+
+
+@pytest.mark.parametrize("num_splits", [0, 7])
+def test_folded_sparse(dev, num_splits):
+    check(_sparse_pairs("sparse_pairs", 35, topk=[512, 0, 77, 1024, 3], stride=1024), dev,
+          num_splits=num_splits, fold_pairs=True)
+
+
+def test_folded_sparse_onehot_probe_is_bit_exact(dev):
+    """The one-hot probe with two query tokens per request: both read the request's index
+    list (q = 0, so both see the same scores) and must give the exact counts."""
+    p, L = _onehot_probe_problem()
+    B = p.B
+    q = np.zeros((2 * B, p.H, p.N + p.R), dtype=np.uint16)
+    p = dataclasses.replace(p, T=2 * B, q=q, row_offsets=(2 * np.arange(B + 1)).astype(np.uint32))
+    d = device_inputs(p, dev)
+    out, lse = run_gpu(p, d, num_splits=0, debug=True, fold_pairs=True)
+    torch.cuda.synchronize()
+    out = out.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy()
+    for b in range(B):
+        J = [int(x) for x in p.indices[b, :int(p.topk_lengths[b])] if x >= 0]
+        counts = np.zeros(L)
+        for r in J:
+            counts[r % L] += 1
+        for t in (2 * b, 2 * b + 1):
+            if J:
+                assert np.array_equal(out[t] * len(J), np.broadcast_to(counts, out[t].shape)), (b, t)
+                assert np.max(np.abs(lse[t] - math.log(len(J)))) < 1e-5
+            else:
+                assert np.all(out[t] == 0) and np.all(np.isneginf(lse[t]))
+
+
 # ------------------------------------------------------------------ full-size workloads
 # the oracle evaluates sampled query tokens (all heads) of the full call, every token the
 # plan splits between partitions among them (all tokens for long context and sparse)
@@ -264,7 +359,7 @@ def _sample(p, k):
     return sorted(set(int(x) for x in st.integers(0, p.T - 1, 4 * k)))[:k]
 
 
-def _split_invariance(p, dev):
+def _split_invariance(p, dev, fold_pairs=None):
     """Every query token of the full call: the launch configuration timed by the benchmark
     (auto splits) against one partition walking the whole batch.  The two round
     differently (other running maxima behind the bf16 P, partials merged in fp32), and
@@ -272,8 +367,8 @@ def _split_invariance(p, dev):
     that tolerance overall and within twice it for every token; a partition dropped or
     counted twice moves a token by far more."""
     d = device_inputs(p, dev)
-    one, _ = run_gpu(p, d, num_splits=1, debug=True)
-    auto, _ = run_gpu(p, d, num_splits=0, debug=True)
+    one, _ = run_gpu(p, d, num_splits=1, debug=True, fold_pairs=fold_pairs)
+    auto, _ = run_gpu(p, d, num_splits=0, debug=True, fold_pairs=fold_pairs)
     torch.cuda.synchronize()
     a, b = auto.float(), one.float()
     assert torch.isfinite(a).all()
@@ -315,3 +410,11 @@ def test_full_sparse(dev):
     p = W.config_sparse()
     check(p, dev)
     _split_invariance(p, dev)
+
+
+def test_full_dsv3_two_tokens_per_request(dev):
+    # multi-token decode on the DeepSeek-V3 shapes: 32 requests x 2 query tokens, both walks
+    p = W.config_dsv3_mtp()
+    for fold in (False, True):
+        check(p, dev, tokens=_sample(p, 16), fold_pairs=fold)
+        _split_invariance(p, dev, fold_pairs=fold)

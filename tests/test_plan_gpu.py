@@ -7,10 +7,10 @@ work, else for equal tile counts), records the token that holds each partition's
 first tile and each token's first and last partition; the split-token counters must
 be back at zero when the call ends (every merge resets the ones it used).
 
-Workspace layout (bytes): plan header (256), TokenPlan[T] (32 each: b, lo, hi,
-tile_first, tile_start, ntiles, part_first, part_last), counters int[T, 4], bounds
-int[2K + 1] (K + 1 bounds, then K first tokens); sections start on 256-byte
-boundaries.
+Workspace layout (bytes): plan header (256), TokenPlan[T] (48 each: b, lo, hi,
+tile_first, tile_start, ntiles, part_first, part_last, own lo, own hi, tokens walked,
+pad), counters int[T, 4], bounds int[2K + 1] (K + 1 bounds, then K first tokens);
+sections start on 256-byte boundaries.
 """
 import numpy as np
 import pytest
@@ -37,10 +37,13 @@ def _up(x):
     return (x + 255) & ~255
 
 
+PLAN_INTS = 12
+
+
 def _read_plan(ws, T, K):
     b = ws.cpu().numpy()
-    plan = b[256:256 + 32 * T].view(np.int32).reshape(T, 8)
-    coff = _up(256 + 32 * T)
+    plan = b[256:256 + 4 * PLAN_INTS * T].view(np.int32).reshape(T, PLAN_INTS)
+    coff = _up(256 + 4 * PLAN_INTS * T)
     counters = b[coff:coff + 16 * T].view(np.int32).reshape(T, 4)
     boff = _up(coff + 16 * T)
     bnd = b[boff:boff + 4 * (2 * K + 1)].view(np.int32)
@@ -105,3 +108,26 @@ def test_plan_even_split_and_empty_partitions(dev):
     p = _config((3000, 1, 2500, 640), "plan_even")
     assert not _check(p, dev, 200, 200)   # more partitions than tiles: empty ones at the end
     _check(p, dev, 9, 9)
+
+
+def test_plan_pairs_tokens_when_folding(dev):
+    """Two query tokens per request: the first of each pair walks the union of both key
+    ranges (causal: the second token's range), the second walks nothing; both keep their
+    own ranges for masking."""
+    lens = [70, 200, 1000, 64]
+    args = dict(W.DSV3, ps=64, cache_lens=lens, qlens=[2] * len(lens),
+                num_pages=sum((n + 63) // 64 for n in lens) + 8, mask=W.MASK_CAUSAL, rms_norm=True)
+    p = W.make_dense("plan_fold", 34, **args)
+    d = device_inputs(p, dev)
+    K = 20
+    ws = torch.zeros(workspace_bytes(p, K), dtype=torch.uint8, device=dev)
+    run_gpu(p, d, num_splits=K, workspace=ws, fold_pairs=True)
+    torch.cuda.synchronize()
+    plan, counters, bnd, _ = _read_plan(ws, p.T, K)
+    lo, hi, nt, mlo, mhi, ntok = plan[:, 1], plan[:, 2], plan[:, 5], plan[:, 8], plan[:, 9], plan[:, 10]
+    for b, n in enumerate(lens):
+        t0, t1 = 2 * b, 2 * b + 1
+        assert (mlo[t0], mhi[t0]) == (0, n - 1) and (mlo[t1], mhi[t1]) == (0, n)
+        assert (lo[t0], hi[t0], ntok[t0]) == (0, n, 2) and nt[t0] == (n + 63) // 64
+        assert nt[t1] == 0 and ntok[t1] == 0
+    assert bnd[K] == int(nt.sum()) and np.all(counters == 0)

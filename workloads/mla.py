@@ -390,6 +390,14 @@ def config_dsv3(seed: int = 1001, B: int = 64, num_pages: int = 40000) -> MlaPro
                       mask=MASK_CAUSAL, rms_norm=True)
 
 
+def config_dsv3_mtp(seed: int = 1006, B: int = 32, qlen: int = 2) -> MlaProblem:
+    """Multi-token decode on the DeepSeek-V3 shapes: B requests x qlen query tokens (a
+    token and its speculative successors), lens U[1024, 8192], causal."""
+    lens = Stream(seed, "dsv3-mtp-lens").integers(1024, 8192, B)
+    return make_dense("dsv3_mtp", seed, **DSV3, ps=64, cache_lens=lens, qlens=[qlen] * B,
+                      num_pages=40000, mask=MASK_CAUSAL, rms_norm=True)
+
+
 def config_long(seed: int = 1002, B: int = 8, window: int = 0) -> MlaProblem:
     """B=8, lens U[32768, 131072]; ``window > 0`` gives the sliding-window-causal variant."""
     lens = Stream(seed, "long-lens").integers(32768, 131072, B)
@@ -412,6 +420,17 @@ def config_sparse(seed: int = 1004, B: int = 128) -> MlaProblem:
     topk = Stream(seed, "sparse-topk").integers(512, 2048, B)
     return make_sparse("sparse", seed, **DSV3, ps=64, tokens_per_request=65536,
                        topk_lengths=topk, stride=2048)
+
+
+def config_sparse_mtp(seed: int = 1007, B: int = 64, qlen: int = 2) -> MlaProblem:
+    """Sparse top-k decode with B requests x qlen query tokens sharing each request's index
+    list (2048 slots, topk_lengths U[512, 2048], 65536 cached tokens per request)."""
+    topk = Stream(seed, "sparse-mtp-topk").integers(512, 2048, B)
+    s = make_sparse("sparse_mtp", seed, **DSV3, ps=64, tokens_per_request=65536, topk_lengths=topk,
+                    stride=2048)
+    T = B * qlen
+    q = to_bf16_bits(Stream(seed, "sparse-mtp-q").normal(T * s.H * (s.N + s.R)).reshape(T, s.H, s.N + s.R))
+    return dataclasses.replace(s, T=T, q=q, row_offsets=(qlen * np.arange(B + 1)).astype(np.uint32))
 
 
 # ----------------------------------------------------------------------------

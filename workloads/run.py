@@ -37,14 +37,15 @@ def device_inputs(p: W.MlaProblem, device) -> dict:
 
 
 def run_gpu(p: W.MlaProblem, d: dict, *, num_splits: int = 0, debug: bool = False, out=None,
-            lse_out=None, workspace=None, stream=None, want_lse: bool = True, timing: bool = False):
+            lse_out=None, workspace=None, stream=None, want_lse: bool = True, timing: bool = False,
+            fold_pairs=None):
     """One library call on prepared device inputs; returns (out bf16 [T,H,V], lse f32 [T,H])."""
     import mla_decode_attention_06_gb300 as M
     dev = d["q"].device
     if want_lse and lse_out is None:
         lse_out = torch.empty((p.T, p.H), dtype=torch.float32, device=dev)
     kw = dict(page_size=p.ps, scale=p.scale, num_splits=num_splits, debug=debug, out=out,
-              lse_out=lse_out, workspace=workspace, stream=stream, timing=timing)
+              lse_out=lse_out, workspace=workspace, stream=stream, timing=timing, fold_pairs=fold_pairs)
     if p.sparse:
         return M.mla_decode_sparse(d["q"], d["offsets"], d["pool"], d["indices"], d["topk"],
                                    d["w_uk"], d["w_uv"], **kw)
