@@ -928,14 +928,20 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         uint8_t* st = sStage + s * C::kStageBytes;
         const bool live = (cs->row_mask[s] >> crow) & 1ull;
         const float sc = live ? a.kv_scales[cs->rowid[s][crow]] : 0.f;
-        uint4 raw[C::RW / 16];
+        // raw[q] holds 16-byte chunk (q + crow) mod RW/16 of the row: rows are RW bytes
+        // apart, so taking the chunks in a rotated order puts eight neighbouring rows'
+        // reads on eight different banks (in order they would all hit the same four)
+        constexpr int kChunks = C::RW / 16;
+        static_assert((kChunks & (kChunks - 1)) == 0, "chunks per row: a power of two");
+        uint4 raw[kChunks];
         const uint8_t* src = st + C::kRawOff + h * 64 * C::RW + crow * C::RW;
 #pragma unroll
-        for (int q = 0; q < C::RW / 16; ++q) raw[q] = *reinterpret_cast<const uint4*>(src + q * 16);
+        for (int q = 0; q < kChunks; ++q)
+          raw[q] = *reinterpret_cast<const uint4*>(src + ((q + crow) & (kChunks - 1)) * 16);
         mbar_arrive(&cs->conv_sync);
         if (h == C::NRH - 1 && !wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
 #pragma unroll
-        for (int q = 0; q < C::RW / 16; ++q) {
+        for (int q = 0; q < kChunks; ++q) {
           const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
           uint32_t o[8];
 #pragma unroll
@@ -943,7 +949,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
             o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
           }
-          const int col = h * C::RW + 16 * q;      // first latent column of this chunk pair
+          const int col = h * C::RW + 16 * ((q + crow) & (kChunks - 1));   // first latent column of the chunk
           uint8_t* box = st + (col >> 6) * C::kBox + crow * 128;
           const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
           *reinterpret_cast<uint4*>(box + (((ch) ^ (crow & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);

@@ -22,6 +22,10 @@
 //     step), the products rounded on their own, the result rounded once to bf16.
 //
 // One block per query token: its threads share the token's heads and the row.
+// Each thread loads a batch of its rotation pairs before it stores any (the
+// compiler cannot tell that q and the tables do not overlap, so a loop that
+// loads, turns and stores one pair at a time waits out a global-memory round
+// trip per pair).
 #include <cstdio>
 
 #include "mla_kernels.cuh"
@@ -29,7 +33,8 @@
 namespace mla {
 namespace pro {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
+constexpr int kBatch = 16;   // rotation pairs a thread loads before it stores
 constexpr int kMaxLatent = 512;
 
 struct Args {
@@ -105,14 +110,14 @@ __device__ __forceinline__ void two_sum(float a, float b, float& hi, float& lo) 
   lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, z)), __fsub_rn(b, z));
 }
 
-// (x0, x1) turned by (c, s): the products of bf16 values are exact in fp32.
-__device__ __forceinline__ void rotate(__nv_bfloat16* x, const __nv_bfloat16* f) {
-  const float x0 = bff(x[0]), x1 = bff(x[1]), c = bff(f[0]), s = bff(f[1]);
+// (x0, x1) turned by (c, s), as bf16 bits: the products of bf16 values are
+// exact in fp32.
+__device__ __forceinline__ void rotate(float x0, float x1, float c, float s, uint16_t& y0, uint16_t& y1) {
   float h0, l0, h1, l1;
   two_sum(__fmul_rn(x0, c), -__fmul_rn(x1, s), h0, l0);
   two_sum(__fmul_rn(x0, s), __fmul_rn(x1, c), h1, l1);
-  x[0] = __ushort_as_bfloat16(round_bf16_pair(h0, l0));
-  x[1] = __ushort_as_bfloat16(round_bf16_pair(h1, l1));
+  y0 = round_bf16_pair(h0, l0);
+  y1 = round_bf16_pair(h1, l1);
 }
 
 __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
@@ -141,10 +146,34 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
     return;
   }
   const __nv_bfloat16* f = a.freqs + (size_t)pos * a.R;
-  // the query's rope part, every head
-  for (int i = tid; i < a.H * (a.R / 2); i += kThreads) {
-    const int h = i / (a.R / 2), pr = i % (a.R / 2);
-    rotate(a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr, f + 2 * pr);
+  // the query's rope part, every head: pair i = (head i / (R/2), pair i % (R/2))
+  const int half = a.R / 2, npairs = a.H * half;
+  for (int i0 = tid; i0 < npairs; i0 += kThreads * kBatch) {
+    float x0[kBatch], x1[kBatch], c[kBatch], sn[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kThreads;
+      if (i < npairs) {
+        const int h = i / half, pr = i % half;
+        const __nv_bfloat16* x = a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr;
+        x0[j] = bff(x[0]);
+        x1[j] = bff(x[1]);
+        c[j] = bff(f[2 * pr]);
+        sn[j] = bff(f[2 * pr + 1]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kThreads;
+      if (i < npairs) {
+        const int h = i / half, pr = i % half;
+        __nv_bfloat16* x = a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr;
+        uint16_t y0, y1;
+        rotate(x0[j], x1[j], c[j], sn[j], y0, y1);
+        x[0] = __ushort_as_bfloat16(y0);
+        x[1] = __ushort_as_bfloat16(y1);
+      }
+    }
   }
   // the row: latent values into shared memory, mean square summed by a tree
   __nv_bfloat16* rp = a.pool + (size_t)row * (a.L + a.R);
@@ -166,7 +195,12 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   const double inv = s_inv;
   for (int l = tid; l < a.L; l += kThreads)
     rp[l] = __ushort_as_bfloat16(round_bf16(__dmul_rn(__dmul_rn(s_lat[l], inv), bf(a.gamma[l]))));
-  for (int pr = tid; pr < a.R / 2; pr += kThreads) rotate(rp + a.L + 2 * pr, f + 2 * pr);
+  for (int pr = tid; pr < half; pr += kThreads) {
+    uint16_t y0, y1;
+    rotate(bff(rp[a.L + 2 * pr]), bff(rp[a.L + 2 * pr + 1]), bff(f[2 * pr]), bff(f[2 * pr + 1]), y0, y1);
+    rp[a.L + 2 * pr] = __ushort_as_bfloat16(y0);
+    rp[a.L + 2 * pr + 1] = __ushort_as_bfloat16(y1);
+  }
 }
 
 }  // namespace pro

@@ -244,12 +244,15 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
         ok = false;
         break;
       }
-      // widen row `tid` of each e4m3 box into the 128B-swizzled bf16 layout
+      // widen row `tid` of each e4m3 box into the 128B-swizzled bf16 layout; a
+      // thread takes its row's eight 8-byte pieces in a rotated order (rows are 64
+      // bytes apart: in order, a half warp's reads would share two banks)
       for (int i = 0; i < MB; ++i) {
         const uint8_t* src = w8_box(s, i) + tid * 64;
         uint8_t* dst = w_box(s, i) + tid * 128;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const int ch = (c8 + tid) & 7;
           const uint2 raw = *reinterpret_cast<const uint2*>(src + ch * 8);
           uint4 v;
           v.x = e4m3x2_to_bf16x2((uint16_t)(raw.x & 0xffff));
