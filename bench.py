@@ -368,13 +368,19 @@ INDEXER_OPS_PER_MAC = 8
 
 
 def time_events(fn, flush, steps, warmup, stream):
+    """Mean device time of fn() over `steps` calls, L2 flushed before each.  A short
+    device-side spin after the flush keeps the GPU busy while the host marshals the
+    call, so the start event is not followed by idle time waiting for the launch."""
     import torch
+    spin = getattr(torch.cuda, "_sleep", None)
     for _ in range(max(3, warmup)):
         flush.zero_()
         fn()
     ev = []
     for _ in range(steps):
         flush.zero_()
+        if spin is not None:
+            spin(200000)   # ~100 us of device time at 2 GHz
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)

@@ -485,8 +485,10 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = CL >= 2 ? cluster_ctarank() : 0u;   // rank in the cluster
-  const uint32_t rank = crank % C::NHALF;                      // latent half of O this CTA owns
-  const int tslot = (int)(crank / C::NHALF);                   // query token slot (folded pairs)
+  // latent half of O this CTA owns, and its query token slot (folded pairs); both
+  // compile-time known where the cluster walks one token
+  const uint32_t rank = C::NSLOT > 1 ? crank % C::NHALF : crank;
+  const int tslot = C::NSLOT > 1 ? (int)(crank / C::NHALF) : 0;
   const int k = blockIdx.x / CL;
   PlanHeader* hdr = a.hdr_mut;
   const int H = a.d.num_heads;

@@ -122,33 +122,53 @@ __device__ __forceinline__ void rotate(float x0, float x1, float c, float s, uin
 
 __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   __shared__ double s_inv;
-  __shared__ double s_lat[kMaxLatent];
   __shared__ double s_part[kThreads / 32];
+  __shared__ long long s_req[4];   // b, first token, end token, cache length of the token's request
   const int t = blockIdx.x, tid = threadIdx.x;
-  // request of token t: the last b with offsets[b] <= t
-  int lo = 0, hi = a.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((int)a.offsets[mid] <= t) lo = mid; else hi = mid - 1;
+  // gamma does not depend on anything: its loads go out first
+  constexpr int kLatPerThread = kMaxLatent / kThreads;
+  double g[kLatPerThread];
+#pragma unroll
+  for (int j = 0; j < kLatPerThread; ++j) {
+    const int l = tid + j * kThreads;
+    g[j] = l < a.L ? bf(a.gamma[l]) : 0.0;
   }
-  const int b = lo;
-  const long long qb = a.offsets[b], qe = a.offsets[b + 1];
-  const long long pos = (long long)a.cache_lens[b] - (qe - qb) + (t - qb);
-  bool ok = qb <= t && t < qe && pos >= 0 && pos < a.max_seq_len && pos < (long long)a.bt_stride * a.ps;
-  long long row = 0;
-  if (ok) {
-    const int page = a.block_table[(size_t)b * a.bt_stride + pos / a.ps];
-    ok = page >= 0 && page < a.num_pages;
-    row = (long long)page * a.ps + pos % a.ps;
+  // the token's request: the b with offsets[b] <= t < offsets[b + 1], found by every
+  // thread testing its own b (one round trip instead of a search's log2(B))
+  if (tid == 0) s_req[0] = -1;
+  __syncthreads();
+  for (int b0 = 0; b0 < a.B; b0 += kThreads) {
+    const int b = b0 + tid;
+    if (b < a.B) {
+      const long long qb = a.offsets[b], qe = a.offsets[b + 1];
+      const long long len = a.cache_lens[b];
+      if (qb <= t && t < qe) {
+        s_req[0] = b;
+        s_req[1] = qb;
+        s_req[2] = qe;
+        s_req[3] = len;
+      }
+    }
   }
+  __syncthreads();
+  const long long bq = s_req[0];
+  bool ok = bq >= 0;
+  const int b = ok ? (int)bq : 0;
+  const long long qb = s_req[1], qe = s_req[2];
+  const long long pos = ok ? s_req[3] - (qe - qb) + (t - qb) : -1;
+  ok = ok && pos >= 0 && pos < a.max_seq_len && pos < (long long)a.bt_stride * a.ps;
   if (!ok) {   // skipped whole, as the decode would drop a bad page; reported
     if (tid == 0) atomicOr(&a.hdr->status, kDeviceCheckFailed);
     return;
   }
+  // the page of the row (needed for the row's loads) and the query's first pairs go
+  // out together; a bad page skips the token whole, before anything is written
+  const int page = a.block_table[(size_t)b * a.bt_stride + pos / a.ps];
   const __nv_bfloat16* f = a.freqs + (size_t)pos * a.R;
   // the query's rope part, every head: pair i = (head i / (R/2), pair i % (R/2))
   const int half = a.R / 2, npairs = a.H * half;
-  for (int i0 = tid; i0 < npairs; i0 += kThreads * kBatch) {
+  bool page_checked = false;
+  for (int i0 = tid; i0 < npairs || !page_checked; i0 += kThreads * kBatch) {
     float x0[kBatch], x1[kBatch], c[kBatch], sn[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
@@ -161,6 +181,13 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
         c[j] = bff(f[2 * pr]);
         sn[j] = bff(f[2 * pr + 1]);
       }
+    }
+    if (!page_checked) {
+      if (page < 0 || page >= a.num_pages) {
+        if (tid == 0) atomicOr(&a.hdr->status, kDeviceCheckFailed);
+        return;
+      }
+      page_checked = true;
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
@@ -175,14 +202,24 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
       }
     }
   }
-  // the row: latent values into shared memory, mean square summed by a tree
-  __nv_bfloat16* rp = a.pool + (size_t)row * (a.L + a.R);
-  double part = 0.0;
-  for (int l = tid; l < a.L; l += kThreads) {
-    const double v = bf(rp[l]);
-    s_lat[l] = v;
-    part = __dadd_rn(part, __dmul_rn(v, v));
+  // the row: latent values and its rope pair read together; mean square summed by a tree
+  __nv_bfloat16* rp = a.pool + ((size_t)page * a.ps + pos % a.ps) * (a.L + a.R);
+  double v[kLatPerThread];
+#pragma unroll
+  for (int j = 0; j < kLatPerThread; ++j) {
+    const int l = tid + j * kThreads;
+    v[j] = l < a.L ? bf(rp[l]) : 0.0;
   }
+  float r0 = 0.f, r1 = 0.f, rc = 0.f, rs = 0.f;
+  if (tid < half) {
+    r0 = bff(rp[a.L + 2 * tid]);
+    r1 = bff(rp[a.L + 2 * tid + 1]);
+    rc = bff(f[2 * tid]);
+    rs = bff(f[2 * tid + 1]);
+  }
+  double part = 0.0;
+#pragma unroll
+  for (int j = 0; j < kLatPerThread; ++j) part = __dadd_rn(part, __dmul_rn(v[j], v[j]));
   for (int o = 16; o > 0; o >>= 1) part = __dadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
   if ((tid & 31) == 0) s_part[tid >> 5] = part;
   __syncthreads();
@@ -193,9 +230,18 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   }
   __syncthreads();
   const double inv = s_inv;
-  for (int l = tid; l < a.L; l += kThreads)
-    rp[l] = __ushort_as_bfloat16(round_bf16(__dmul_rn(__dmul_rn(s_lat[l], inv), bf(a.gamma[l]))));
-  for (int pr = tid; pr < half; pr += kThreads) {
+#pragma unroll
+  for (int j = 0; j < kLatPerThread; ++j) {
+    const int l = tid + j * kThreads;
+    if (l < a.L) rp[l] = __ushort_as_bfloat16(round_bf16(__dmul_rn(__dmul_rn(v[j], inv), g[j])));
+  }
+  if (tid < half) {
+    uint16_t y0, y1;
+    rotate(r0, r1, rc, rs, y0, y1);
+    rp[a.L + 2 * tid] = __ushort_as_bfloat16(y0);
+    rp[a.L + 2 * tid + 1] = __ushort_as_bfloat16(y1);
+  }
+  for (int pr = tid + kThreads; pr < half; pr += kThreads) {   // rope wider than 2 x threads
     uint16_t y0, y1;
     rotate(bff(rp[a.L + 2 * pr]), bff(rp[a.L + 2 * pr + 1]), bff(f[2 * pr]), bff(f[2 * pr + 1]), y0, y1);
     rp[a.L + 2 * pr] = __ushort_as_bfloat16(y0);
