@@ -149,7 +149,8 @@ int mla_decode_paged(const mla_dims_t* dims, const mla_opts_t* opts, const void*
  * mla_decode_branch_fp8 page: w_uk_scale, w_uv_scale with block granularity).
  *   kv_pool_fp8   bytes [num_pages, ps, L + 2R]: L e4m3 (OCP E4M3FN) c_kv codes,
  *                 then R bf16 k_rope values; c_kv = code * kv_scales[row]
- *   kv_scales     float [num_pages, ps]
+ *   kv_scales     float [num_pages, ps], 16-byte aligned (a page's scales are
+ *                 copied into shared memory with its rows)
  *   w_uk_fp8      e4m3 [H, L, N], w_uk_scale float [H, ceil(L/128), ceil(N/128)]
  *   w_uv_fp8      e4m3 [H, V, L], w_uv_scale float [H, ceil(V/128), ceil(L/128)]
  *   q_scale       must be NULL (sigma_Q = 1, the decode page's default)

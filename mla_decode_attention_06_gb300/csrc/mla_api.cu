@@ -299,7 +299,7 @@ int mla_decode_paged_fp8(const mla_dims_t* dims, const mla_opts_t* opts, const v
                          size_t workspace_bytes, void* stream) {
   if (q_scale) return MLA_ERR_UNSUPPORTED;
   if (!dims || !block_table || !cache_lens || block_table_stride < 1 || !kv_scales || !w_uk_scale ||
-      !w_uv_scale)
+      !w_uv_scale || !aligned16(kv_scales))
     return MLA_ERR_INVALID_ARG;
   CallCommon c{};
   c.d = dims;

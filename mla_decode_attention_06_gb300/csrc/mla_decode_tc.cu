@@ -81,7 +81,9 @@ struct Smem {   // control block after the stage ring
   uint64_t fix_bar, fix_done;    // softmax: partial written / claim outcome published
   uint64_t mrg_full[2], mrg_done[2];   // merge: a half partial landed in its buffer / was read
   uint64_t bye;                  // the other CTAs are done touching this CTA's shared memory
-  int32_t rowid[kMaxStages][64]; // physical row of each tile row (kLoadFp8, kLoadSparse)
+  // kLoadSparse: physical row of each tile row; kLoadFp8: each tile row's scale (fp32
+  // bits), copied in with the tile
+  alignas(16) int32_t rowid[kMaxStages][64];
   uint32_t tmem_base;
   int abort;
   int fix_last;   // this CTA merges the split token it just finished (it claimed it last)
@@ -690,7 +692,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (c >= S && !wwait(&cs->kv_empty[s], ((c / S) & 1) ^ 1, cs, hdr)) return;
         if (MODE == kLoadDense) finish(it, raw, v, rid, pg);
         if (pf) finish(it + kPrefetchAhead, raw2, v2, rid2, pg2);
-        if (MODE != kLoadDense) {
+        if (MODE == kLoadSparse) {
           cs->rowid[s][lane] = rid[0];
           cs->rowid[s][lane + 32] = rid[1];
         }
@@ -731,8 +733,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           }
         } else {
           // pages of this tile that hold at least one live row; both CTAs count the
-          // same bytes, most of which the other CTAs' multicasts deliver
-          const uint32_t row_bytes = (MODE == kLoadFp8 ? L : C::NLB * 128) + 128;
+          // same bytes, most of which the other CTAs' multicasts deliver (an e4m3 row's
+          // 4-byte scale each CTA copies for itself)
+          const uint32_t row_bytes = (MODE == kLoadFp8 ? L + 4 : C::NLB * 128) + 128;
           uint32_t live_rows = 0;
           for (int p = 0; p < nloads; ++p)
             if ((mask >> (p * rows_per_load)) & lmask) live_rows += rows_per_load;
@@ -757,6 +760,10 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
               }
             } else if (lane == kOwn && crank == 0) {
               load_box(st_rope + r0 * 128, &maps.kv_rope, &cs->kv_full[s], rope_x0, y);
+            } else if (MODE == kLoadFp8 && lane == kOwn + 1) {
+              // the load's row scales: rows y .. y + rows_per_load - 1 are consecutive
+              // (one page), y a multiple of 8, so the copy is 16-byte aligned
+              bulk_copy_g2s(&cs->rowid[s][r0], a.kv_scales + y, (uint32_t)rows_per_load * 4, &cs->kv_full[s]);
             }
           }
           if (pf) {
@@ -915,12 +922,18 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
     });
   } else if (MODE == kLoadFp8 && warp >= 6) {
     // ------------------------------------------------------------- e4m3 converters
-    // thread ci widens raw box h = ci / 64 of tile row ci % 64: RW e4m3 codes x
-    // row scale -> bf16 in the 128B-swizzled latent boxes; dead rows become zeros
-    // (latent and rope).  The codes sit where the last raw box's latent boxes go
-    // (L = 512: boxes 4-7; L = 64: box 0), so the threads writing those boxes
-    // wait until every thread has read its codes.
-    const int ci = tid - 192, crow = ci & 63, h = ci >> 6;
+    // Tile row crow = ci % 64 is widened by NRH threads, thread hh = ci / 64 taking
+    // the hh-th RW / NRH bytes of each raw box: e4m3 code x row scale -> bf16 in the
+    // 128B-swizzled latent boxes, raw box p after raw box p - 1; dead rows become
+    // zeros (latent and rope).  The codes sit where the last raw box's latent boxes
+    // go (L = 512: boxes 4-7; L = 64: box 0), so the last pass writes only after
+    // every thread has read its codes; earlier passes write boxes that hold none.
+    // A pass holds only its part of the row in registers.  The row scales come
+    // into shared memory with the tile (the producer copies them asynchronously).
+    const int ci = tid - 192, crow = ci & 63, hh = ci >> 6;
+    constexpr int kPart = C::RW / C::NRH;          // bytes of a raw box row per thread
+    constexpr int kChunks = kPart / 16;
+    static_assert(kChunks >= 1 && (kChunks & (kChunks - 1)) == 0, "chunks per part: a power of two");
     int c = 0;
     for_each_segment(a, k, g0, g1, [&](int si, int t, const TokenPlan& tp, int ia, int ie, bool, int) {
       for (int it = ia; it < ie; ++it, ++c) {
@@ -929,35 +942,39 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         if (!wwait(&cs->kv_full[s], (c / S) & 1, cs, hdr)) return;
         uint8_t* st = sStage + s * C::kStageBytes;
         const bool live = (cs->row_mask[s] >> crow) & 1ull;
-        const float sc = live ? a.kv_scales[cs->rowid[s][crow]] : 0.f;
-        // raw[q] holds 16-byte chunk (q + crow) mod RW/16 of the row: rows are RW bytes
-        // apart, so taking the chunks in a rotated order puts eight neighbouring rows'
-        // reads on eight different banks (in order they would all hit the same four)
-        constexpr int kChunks = C::RW / 16;
-        static_assert((kChunks & (kChunks - 1)) == 0, "chunks per row: a power of two");
-        uint4 raw[kChunks];
-        const uint8_t* src = st + C::kRawOff + h * 64 * C::RW + crow * C::RW;
+        const float sc = live ? __int_as_float(cs->rowid[s][crow]) : 0.f;
+#pragma unroll 1
+        for (int p = 0; p < C::NRH; ++p) {
+          // raw[q] holds 16-byte chunk (q + crow) mod kChunks of this thread's part: rows
+          // are RW bytes apart, so the rotation puts eight neighbouring rows' reads on
+          // eight different banks (in order they would all hit the same ones)
+          uint4 raw[kChunks];
+          const uint8_t* src = st + C::kRawOff + p * 64 * C::RW + crow * C::RW + hh * kPart;
 #pragma unroll
-        for (int q = 0; q < kChunks; ++q)
-          raw[q] = *reinterpret_cast<const uint4*>(src + ((q + crow) & (kChunks - 1)) * 16);
-        mbar_arrive(&cs->conv_sync);
-        if (h == C::NRH - 1 && !wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
-#pragma unroll
-        for (int q = 0; q < kChunks; ++q) {
-          const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
-          uint32_t o[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
-            o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
+          for (int q = 0; q < kChunks; ++q)
+            raw[q] = *reinterpret_cast<const uint4*>(src + ((q + crow) & (kChunks - 1)) * 16);
+          if (p == C::NRH - 1) {
+            mbar_arrive(&cs->conv_sync);
+            if (!wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
           }
-          const int col = h * C::RW + 16 * ((q + crow) & (kChunks - 1));   // first latent column of the chunk
-          uint8_t* box = st + (col >> 6) * C::kBox + crow * 128;
-          const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
-          *reinterpret_cast<uint4*>(box + (((ch) ^ (crow & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (crow & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+          for (int q = 0; q < kChunks; ++q) {
+            const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
+              o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
+            }
+            // first latent column of the chunk
+            const int col = p * C::RW + hh * kPart + 16 * ((q + crow) & (kChunks - 1));
+            uint8_t* box = st + (col >> 6) * C::kBox + crow * 128;
+            const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
+            *reinterpret_cast<uint4*>(box + (((ch) ^ (crow & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (crow & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
         }
-        if (!live && h == 0) {
+        if (!live && hh == 0) {
           uint4* rr = reinterpret_cast<uint4*>(st + C::NLB * C::kBox + crow * 128);
 #pragma unroll
           for (int i = 0; i < 8; ++i) rr[i] = make_uint4(0, 0, 0, 0);

@@ -120,6 +120,14 @@ def test_fp8_q_scale_and_sparse_mask_are_unsupported(lib):
     assert rc == 2
 
 
+def test_fp8_row_scales_must_be_16_byte_aligned(lib):
+    # a page's row scales are copied into shared memory by the bulk-copy engine
+    rc = lib.mla_decode_paged_fp8(ctypes.byref(_dims()), ctypes.byref(_opts()), FAKE, FAKE, 2, 2,
+                                  FAKE, FAKE + 4, FAKE, 4, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                  None, FAKE, 1 << 40, None)
+    assert rc == 1
+
+
 def _expected_workspace(H, L, R, T, K, NI=1):
     """The workspace sections in order, each starting on a 256-byte boundary:
     plan header, TokenPlan[T] (48 bytes), counters int[T, 4], bounds int[2K + 1],
