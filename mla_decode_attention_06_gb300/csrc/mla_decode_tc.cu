@@ -72,6 +72,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 struct Smem {   // control block after the stage ring
   uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
   uint64_t kv_conv[kMaxStages];  // e4m3 rows widened (kLoadFp8)
+  uint64_t kv_conv_a[kMaxStages];  // ... their first raw box (latent [0, RW)), when NRH > 1
   uint64_t row_mask[kMaxStages];
   uint64_t q_full, q_empty;
   uint64_t qa_full, qa_done;     // query latent [0, QT) staged in shared memory / moved into TMEM
@@ -124,6 +125,7 @@ struct Cfg {
   static_assert(kQCol + QT / 2 <= 512, "TMEM columns");
   static_assert(kStgBytes + 2 * kMrgHalf <= kRegionBytes, "merge buffers in the idle region");
   static_assert(kMode != kLoadFp8 || NRH % CL == 0, "raw boxes split over the cluster");
+  static_assert(kMode != kLoadFp8 || NRH == 1 || QT == RW, "raw box 0 is the QK's TMEM-operand part");
   static_assert(QT / 64 <= NQS + 1, "the query staging fits the query buffer");
   static_assert(kSmem <= 232448, "shared memory");
 };
@@ -504,6 +506,7 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
       mbar_init(&cs->kv_full[s], 1);
       mbar_init(&cs->kv_empty[s], CL);   // one tcgen05.commit from each CTA of the cluster
       mbar_init(&cs->kv_conv[s], C::kConvThreads);
+      mbar_init(&cs->kv_conv_a[s], C::kConvThreads);
     }
     mbar_init(&cs->q_full, 1 + 128);     // producer (TMA bytes) + every softmax thread (TMEM part)
     mbar_init(&cs->q_empty, 1);
@@ -829,7 +832,9 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         const int s = cq % S, b = cq & 1;
         const uint32_t par = (cq / S) & 1;
         if (cq >= 2 && !wwait(&cs->pv_done[b], ((cq - 2) >> 1) & 1, cs, hdr)) return;
-        if (!wwait(MODE == kLoadFp8 ? &cs->kv_conv[s] : &cs->kv_full[s], par, cs, hdr)) return;
+        if (!wwait(MODE != kLoadFp8 ? &cs->kv_full[s] : C::NRH > 1 ? &cs->kv_conv_a[s] : &cs->kv_conv[s], par, cs,
+                   hdr))
+          return;
         const uint64_t mask = cs->row_mask[s];
         if (MODE != kLoadFp8 && mask != ~0ull) {
           // Rows outside the key range may hold anything (NaN included).  Their
@@ -870,6 +875,12 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
           if (!wwait(&cs->q_full, si & 1, cs, hdr)) return;
           tc_fence_after();
           q_smem = true;
+        }
+        if (MODE == kLoadFp8 && C::NRH > 1) {
+          // the rest of the tile's latent columns and the dead rows' rope zeros
+          __syncwarp();
+          if (!wwait(&cs->kv_conv[s], par, cs, hdr)) return;
+          tc_fence_after();
         }
         if (lane == 0) {
 #pragma unroll 1
@@ -972,6 +983,11 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
             *reinterpret_cast<uint4*>(box + (((ch) ^ (crow & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (crow & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          if (C::NRH > 1 && p == 0) {
+            // latent [0, RW) is in place: the QK's TMEM-operand part may start
+            fence_proxy_async_smem();
+            mbar_arrive(&cs->kv_conv_a[s]);
           }
         }
         if (!live && hh == 0) {

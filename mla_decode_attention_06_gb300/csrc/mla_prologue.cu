@@ -21,7 +21,9 @@
 //     sums of any order differ in the last bits only, far below the bf16 rounding
 //     step), the products rounded on their own, the result rounded once to bf16.
 //
-// One block per query token: its threads share the token's heads and the row.
+// A token's heads are shared by G blocks (blockIdx.y = 0 .. G-1, G chosen so the
+// grid covers the SMs about twice); block 0 of each token also normalises the
+// cache row.
 // Each thread loads a batch of its rotation pairs before it stores any (the
 // compiler cannot tell that q and the tables do not overlap, so a loop that
 // loads, turns and stores one pair at a time waits out a global-memory round
@@ -125,13 +127,14 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   __shared__ double s_part[kThreads / 32];
   __shared__ long long s_req[4];   // b, first token, end token, cache length of the token's request
   const int t = blockIdx.x, tid = threadIdx.x;
+  const bool row_block = blockIdx.y == 0;   // this block also normalises the cache row
   // gamma does not depend on anything: its loads go out first
   constexpr int kLatPerThread = kMaxLatent / kThreads;
   double g[kLatPerThread];
 #pragma unroll
   for (int j = 0; j < kLatPerThread; ++j) {
     const int l = tid + j * kThreads;
-    g[j] = l < a.L ? bf(a.gamma[l]) : 0.0;
+    g[j] = row_block && l < a.L ? bf(a.gamma[l]) : 0.0;
   }
   // the token's request: the b with offsets[b] <= t < offsets[b + 1], found by every
   // thread testing its own b (one round trip instead of a search's log2(B))
@@ -165,8 +168,11 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   // out together; a bad page skips the token whole, before anything is written
   const int page = a.block_table[(size_t)b * a.bt_stride + pos / a.ps];
   const __nv_bfloat16* f = a.freqs + (size_t)pos * a.R;
-  // the query's rope part, every head: pair i = (head i / (R/2), pair i % (R/2))
-  const int half = a.R / 2, npairs = a.H * half;
+  // the query's rope part, this block's heads [h0, h1): pair i = (head h0 + i / (R/2),
+  // pair i % (R/2))
+  const int half = a.R / 2;
+  const int h0 = (int)((long long)blockIdx.y * a.H / gridDim.y), h1 = (int)((long long)(blockIdx.y + 1) * a.H / gridDim.y);
+  const int npairs = (h1 - h0) * half;
   bool page_checked = false;
   for (int i0 = tid; i0 < npairs || !page_checked; i0 += kThreads * kBatch) {
     float x0[kBatch], x1[kBatch], c[kBatch], sn[kBatch];
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
     for (int j = 0; j < kBatch; ++j) {
       const int i = i0 + j * kThreads;
       if (i < npairs) {
-        const int h = i / half, pr = i % half;
+        const int h = h0 + i / half, pr = i % half;
         const __nv_bfloat16* x = a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr;
         x0[j] = bff(x[0]);
         x1[j] = bff(x[1]);
@@ -193,7 +199,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
     for (int j = 0; j < kBatch; ++j) {
       const int i = i0 + j * kThreads;
       if (i < npairs) {
-        const int h = i / half, pr = i % half;
+        const int h = h0 + i / half, pr = i % half;
         __nv_bfloat16* x = a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr;
         uint16_t y0, y1;
         rotate(x0[j], x1[j], c[j], sn[j], y0, y1);
@@ -202,6 +208,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
       }
     }
   }
+  if (!row_block) return;
   // the row: latent values and its rope pair read together; mean square summed by a tree
   __nv_bfloat16* rp = a.pool + ((size_t)page * a.ps + pos % a.ps) * (a.L + a.R);
   double v[kLatPerThread];
@@ -276,7 +283,15 @@ cudaError_t launch_prologue(const mla_dims_t& d, void* q, const uint32_t* offset
   a.freqs = static_cast<const __nv_bfloat16*>(freqs);
   a.gamma = static_cast<const __nv_bfloat16*>(gamma);
   a.hdr = hdr;
-  pro::prologue_kernel<<<T, pro::kThreads, 0, s>>>(a);
+  // blocks per token: the grid covers the SMs about twice, at least one head each
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  int G = (2 * sms + T - 1) / T;
+  if (G > a.H) G = a.H;
+  if (G > 65535) G = 65535;
+  if (G < 1) G = 1;
+  pro::prologue_kernel<<<dim3(T, G), pro::kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
