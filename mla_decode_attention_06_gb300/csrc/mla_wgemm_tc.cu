@@ -119,6 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   const uint32_t tcols = ncols_needed <= 32 ? 32 : ncols_needed <= 64 ? 64 : ncols_needed <= 128 ? 128
                          : ncols_needed <= 256 ? 256 : 512;
 
+  auto load_w = [&](int kb) {
+    const int s = kb % S;
+    for (int i = 0; i < MB; ++i)
+      tma_load_2d(kFp8 ? w8_box(s, i) : w_box(s, i), &maps.w, &full[s], kb * 64, h * a.M + 128 * (mb0 + i));
+  };
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -126,7 +131,12 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
     }
     mbar_init(done, 1);
     fence_mbar_init();
-    prefetch_tensormap(&maps.w);
+    // the weights depend neither on the previous kernel nor on TMEM: they start
+    // streaming before the allocation and the block-wide sync
+    for (int kb = 0; kb < nkb && kb < S; ++kb) {
+      mbar_arrive_expect_tx(&full[kb], stage_tx);
+      load_w(kb);
+    }
     prefetch_tensormap(&maps.x);
   }
   if (warp == 0) {
@@ -138,11 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  auto load_w = [&](int kb) {
-    const int s = kb % S;
-    for (int i = 0; i < MB; ++i)
-      tma_load_2d(kFp8 ? w8_box(s, i) : w_box(s, i), &maps.w, &full[s], kb * 64, h * a.M + 128 * (mb0 + i));
-  };
   auto load_x = [&](int kb) {
     const int s = kb % S;
     asm volatile(
@@ -151,12 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1) wgemm_kernel(const __grid_constan
         "l"(reinterpret_cast<uint64_t>(&maps.x)), "r"(smem_u32(&full[s])), "r"(kb * 64), "r"(h), "r"(t0)
         : "memory");
   };
-  // weights do not depend on the previous kernel: start streaming them first
-  if (tid == 0)
-    for (int kb = 0; kb < nkb && kb < S; ++kb) {
-      mbar_arrive_expect_tx(&full[kb], stage_tx);
-      load_w(kb);
-    }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");   // q (absorb) / o_lat, lse of the decode (W_uv)
   if (tid == 0)
