@@ -256,14 +256,11 @@ __device__ __forceinline__ size_t part_index(int k, int slot, int c, int row, in
   return ((size_t)(k * 2 * ns + slot) * (L / 4) + c) * H + row;
 }
 
-// Log-sum-exp merge of one split token's partials for head `row`, latent
-// columns [lat_x0, lat_x0 + LC):  lse = ln sum_p e^{lse_p},
-// o = sum_p e^{lse_p - lse} o_p.  Partitions with an empty key set carry
-// lse_p = -inf and drop out.  Partition k holds the token in slot 0 (its
-// first segment) unless the token began inside partition kf's range.  This is
-// the general form, every partial read from global memory; the common case
-// (the merging CTA's own partial still in TMEM, its stage ring idle) runs in
-// the softmax epilogue instead.
+// The merge of merge_in_tmem (below) with per-thread loads instead of bulk
+// copies, every partial read from global memory: the e4m3 instance merges an
+// earlier segment's token this way (measured faster there; the bf16 instances
+// use merge_in_tmem with no partial in TMEM).  Same operations in the same
+// order, so the bits are the same.
 __device__ __noinline__ void merge_split_token(const DecodeArgs& a, int t, const TokenPlan& tp, int kf, int kl,
                                                int slot_kf, uint32_t rank, int row, int lat_x0, int LC, int ns,
                                                int ts) {
@@ -319,18 +316,24 @@ __device__ __forceinline__ bool wwait_cluster(uint64_t* bar, uint32_t parity, Sm
 }
 __device__ __forceinline__ bool waborted(const Smem* cs) { return __any_sync(0xffffffffu, aborted(cs)); }
 
-// The merge of a split token by a CTA whose last segment it was: O in TMEM
-// still holds this CTA's own partial (unnormalised; 1 / row sum = inv) and the
-// query buffer and stage ring are idle.  Each other partition's slice of its
-// partial (one contiguous block of the interleaved layout) comes in as two
-// halves of LC / 2 columns by bulk copy, double-buffered at the end of the idle
-// region, the first two issued before the weights are known.  acc = sum over
-// partitions, in order, of fmaf(w_p, o_p, acc) from zero: the operations and
-// order of merge_split_token, so the bits do not depend on which partition
-// merges.  acc lives in TMEM at `tacc` (the S and query columns, idle after
-// the last QK).  Each thread stages its own bf16 output row at the start of the
-// region (rows padded by 16 bytes) and writes it with one bulk copy.
-// Warp-uniform; false on a time-out.
+// Log-sum-exp merge of one split token's partials for head `row`, latent
+// columns [lat_x0, lat_x0 + LC):  lse = ln sum_p e^{lse_p},
+// o = sum_p e^{lse_p - lse} o_p.  Partitions with an empty key set carry
+// lse_p = -inf and drop out.  Partition kf holds the token in slot 1 (its last
+// segment) if the token began inside its range, every other partition in slot 0.
+// Run by the last partition to claim the token, after its own final segment,
+// when the query buffer and stage ring are idle.  If the token is that final
+// segment's (k in [kf, kl]), O in TMEM still holds this CTA's own partial
+// (unnormalised; 1 / row sum = inv); otherwise (k = -1: a token of the CTA's
+// first segment) every partial is in global memory.  Each partial's slice
+// (one contiguous block of the interleaved layout) comes in as two halves of
+// LC / 2 columns by bulk copy, double-buffered at the end of the idle region,
+// the first two issued before the weights are known.  acc = sum over
+// partitions, in order, of fmaf(w_p, o_p, acc) from zero, whichever partition
+// merges, so the bits do not depend on it.  acc lives in TMEM at `tacc` (the S
+// and query columns, idle after the last QK).  Each thread stages its own bf16
+// output row at the start of the region (rows padded by 16 bytes) and writes it
+// with one bulk copy.  Warp-uniform; false on a time-out.
 template <int LC>
 __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t, const TokenPlan& tp, int k, int kf,
                                            int kl, int slot_kf, uint32_t rank, int row, int lat_x0, uint32_t trow,
@@ -345,13 +348,14 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
   auto slot_of = [&](int kk) { return (kk == kf ? slot_kf : 0) * ns + ts; };
   auto lse_ptr = [&](int kk) { return a.part_lse + ((size_t)(kk * 2 * ns + slot_of(kk)) * 2 + rank) * H + row; };
   const int np = kl - kf + 1;
-  const int nj = 2 * (np - 1);                          // half slices to bring in
+  const bool own = k >= kf && k <= kl;                  // this CTA's partial is in TMEM (O)
+  const int nj = 2 * (np - (own ? 1 : 0));              // half slices to bring in
   const uint32_t half_bytes = (uint32_t)(LH * H * 4);
   auto issue = [&](int j) {                             // thread row 0: bring in half slice j
     const int g = nmrg + j, b = g & 1;
     if (g >= 2 && !wait_or_abort(&cs->mrg_done[b], ((g - 2) >> 1) & 1, cs, hdr)) return false;
     int p = kf + (j >> 1);
-    if (p >= k) ++p;
+    if (own && p >= k) ++p;
     mbar_arrive_expect_tx(&cs->mrg_full[b], half_bytes);
     bulk_copy_g2s(hb + b * kHalf,
                   reinterpret_cast<const float4*>(a.part_o) +
@@ -366,8 +370,8 @@ __device__ __noinline__ bool merge_in_tmem(const DecodeArgs& a, Smem* cs, int t,
     if (ok && nj > 1) ok = issue(1);
   }
   if (!__all_sync(0xffffffffu, ok)) return false;
-  // max, then sum over p in order of e^(lse_p - max), as the general form does;
-  // up to eight partitions' log-sum-exps are loaded once, eight at a time
+  // max, then sum over p in order of e^(lse_p - max); up to eight partitions'
+  // log-sum-exps are loaded once, eight at a time
   float lv0[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -1306,8 +1310,18 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
         mbar_arrive(&cs->fix_done);
       }
       if (wwait(&cs->fix_done, nfix & 1, cs, hdr) && !waborted(cs) && cs->fix_last) {
-        if (row < H) merge_split_token(a, pend_t, pend_tp, kf, kl, slot_kf, rank, row, lat_x0, LC, C::NSLOT, tslot);
-        if (row == 0) {
+        // the final segment is done: query buffer, stage ring and TMEM S / query
+        // columns are idle; no partial of this token is in TMEM
+        // (a time-out inside has set the abort flag; the threads go on to the teardown)
+        bool merged = true;
+        if constexpr (MODE == kLoadFp8) {
+          if (row < H) merge_split_token(a, pend_t, pend_tp, kf, kl, slot_kf, rank, row, lat_x0, LC, C::NSLOT, tslot);
+        } else {
+          merged = merge_in_tmem<LC>(a, cs, pend_t, pend_tp, -1, kf, kl, slot_kf, rank, row, lat_x0, trow,
+                                     trow + C::kSCol, 0.f, 0.f, sQ, sQ + C::kRegionBytes - 2 * C::kMrgHalf, nmrg,
+                                     C::NSLOT, tslot);
+        }
+        if (merged && row == 0) {
           a.counters[4 * pend_t + rank] = 0;
           a.counters[4 * pend_t + 2 + rank] = 0;
         }
