@@ -193,16 +193,21 @@ int mla_decode_sparse(const mla_dims_t* dims, const mla_opts_t* opts, const void
  *     latent part c -> c / sqrt(mean(c^2) + epsilon) * kv_norm_gamma, rope part
  *     turned like the query's;
  *   - no other value changes.
- * Every result is the double-precision value of those expressions (each product
- * and sum rounded separately, the mean square summed in latent order) rounded
- * once to bf16, nearest with ties to even.
- *   q              bf16 [T, H, N+R], rope part rewritten in place
- *   kv_pool        bf16 [num_pages, ps, L+R] (L <= 512), rows rewritten in place
- *   freqs_cis      bf16 [max_seq_len, R]: per position R/2 (cos, sin) pairs
+ * Every result is the value of those expressions, evaluated in double precision,
+ * rounded once to bf16, nearest with ties to even (the rotations exactly; the
+ * RMSNorm within a few double-precision units of the last place, so a result
+ * can differ from the correctly rounded one only when the exact value lies that
+ * close to a bf16 halfway point).
+ *   q              bf16 [T, H, N+R], rope part rewritten in place; 4-byte aligned
+ *   kv_pool        bf16 [num_pages, ps, L+R] (L <= 512), rows rewritten in place;
+ *                  4-byte aligned
+ *   freqs_cis      bf16 [max_seq_len, R]: per position R/2 (cos, sin) pairs;
+ *                  4-byte aligned
  *   kv_norm_gamma  bf16 [L]
  *   epsilon        >= 0
  *   flags          0 or MLA_FLAG_DEBUG_CHECKS (wait and report device checks)
- *   workspace      device memory, >= 256 bytes, 16-byte aligned (status word)
+ *   workspace      device memory, >= 256 bytes, 16-byte aligned (status word;
+ *                  cleared and read back in debug mode only)
  * Other arguments as mla_decode_paged.  A token whose position is outside
  * [0, max_seq_len) or whose page id is outside [0, num_pages) is left unchanged
  * (query and row) and recorded: MLA_ERR_DEVICE_CHECK in debug mode. */

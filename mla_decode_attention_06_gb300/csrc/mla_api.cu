@@ -390,11 +390,16 @@ int mla_branch_prologue(const mla_dims_t* dims, void* q, const uint32_t* input_r
   if (!q || !input_row_offsets || !kv_pool || !block_table || !cache_lens || !freqs_cis || !kv_norm_gamma ||
       !workspace)
     return MLA_ERR_INVALID_ARG;
+  // rotation pairs are read and written as 4-byte words
+  auto aligned4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!aligned4(q) || !aligned4(kv_pool) || !aligned4(freqs_cis)) return MLA_ERR_INVALID_ARG;
   if (!(epsilon >= 0.f) || (flags & ~MLA_FLAG_DEBUG_CHECKS)) return MLA_ERR_INVALID_ARG;
   if (workspace_bytes < sizeof(PlanHeader) || !aligned16(workspace)) return MLA_ERR_WORKSPACE_TOO_SMALL;
   PlanHeader* hdr = static_cast<PlanHeader*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), s) != cudaSuccess) return MLA_ERR_CUDA;
+  // the status word is read back only in debug mode, so only then is it cleared first
+  if ((flags & MLA_FLAG_DEBUG_CHECKS) && cudaMemsetAsync(hdr, 0, sizeof(PlanHeader), s) != cudaSuccess)
+    return MLA_ERR_CUDA;
   const cudaError_t e = launch_prologue(*dims, q, input_row_offsets, batch, total_q, kv_pool, block_table,
                                         block_table_stride, cache_lens, freqs_cis, max_seq_len, kv_norm_gamma,
                                         epsilon, hdr, s);
@@ -441,8 +446,7 @@ int mla_indexer_fp8(int32_t num_heads, int32_t head_dim, int32_t page_size, int3
   if (top_k > kIndexerMaxTopK) return MLA_ERR_UNSUPPORTED;
   if ((int64_t)num_pages * page_size > INT32_MAX || (int64_t)block_table_stride * page_size > INT32_MAX)
     return MLA_ERR_UNSUPPORTED;
-  const size_t score_smem = ((size_t)num_heads + 32) * (head_dim + 1) * 4 + num_heads + 48 +
-                            (size_t)32 * num_heads * 8;
+  const size_t score_smem = indexer_scores_smem(num_heads, head_dim);
   if (num_heads > 128 || score_smem > kIndexerMaxScoreSmem) return MLA_ERR_UNSUPPORTED;
   if (!q || !q_s || !input_row_offsets || !k_cache || !k_scales || !block_table || !cache_lens ||
       !output_indices || !workspace)

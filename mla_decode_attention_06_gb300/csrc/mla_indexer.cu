@@ -34,6 +34,18 @@ namespace mla {
 namespace idx {
 
 constexpr int kKeysPerBlock = 32;
+
+// Row pitch (ints) of the staged query and key values: D rounded up to a multiple
+// of 4 (16-byte loads, rows 16-byte aligned), plus 4 more when that is a multiple
+// of 8 ints (so eight consecutive rows start in eight different bank groups).
+__host__ __device__ inline int padded_dims(int D) {
+  const int c4 = (D + 3) / 4;
+  return 4 * (c4 % 2 == 0 ? c4 + 1 : c4);
+}
+// Byte offset of the dot-product block after the staged values and NaN flags.
+__host__ __device__ inline size_t dots_offset(int H, int D) {
+  return ((((size_t)H + kKeysPerBlock) * padded_dims(D) * 4 + H + kKeysPerBlock + 15) & ~(size_t)15);
+}
 constexpr int kScoreThreads = 256;
 constexpr int kSelectThreads = 1024;
 constexpr unsigned long long kInvalidKey = ~0ull;        // a key whose page id is out of range
@@ -114,16 +126,19 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
   if (j0 >= n) return;
   const int nk = min(kKeysPerBlock, n - j0);
   const int HD = a.H * a.D;
-  const int DP = a.D + 1;                                  // padded rows: no bank conflicts
+  const int DP = padded_dims(a.D);                         // row pitch in ints (see padded_dims)
   int* qv = reinterpret_cast<int*>(sm);                    // [H][DP] query values x 2^9
   int* kv = qv + a.H * DP;                                 // [32][DP] key values x 2^9
   uint8_t* qnan = reinterpret_cast<uint8_t*>(kv + kKeysPerBlock * DP);   // [H]
   uint8_t* knan = qnan + a.H;                                            // [32]
-  long long* dots = reinterpret_cast<long long*>(sm + ((((size_t)a.H + kKeysPerBlock) * DP * 4 + a.H + kKeysPerBlock + 15) & ~(size_t)15));
+  long long* dots = reinterpret_cast<long long*>(sm + dots_offset(a.H, a.D));
   __shared__ long long rows_s[kKeysPerBlock];
   __shared__ int bad_s;
   if (tid == 0) bad_s = 0;
   for (int i = tid; i < a.H; i += kScoreThreads) qnan[i] = 0;
+  // padding columns [D, DP) of every row hold zeros (the inner loop reads 4 at a time)
+  for (int i = tid; i < (a.H + kKeysPerBlock) * (DP - a.D); i += kScoreThreads)
+    qv[(i / (DP - a.D)) * DP + a.D + i % (DP - a.D)] = 0;
   if (tid < kKeysPerBlock) knan[tid] = 0;
   __syncthreads();
   for (int i = tid; i < HD; i += kScoreThreads) {
@@ -160,14 +175,19 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
       for (int y = 0; y < 8; ++y) acc[x][y] = 0;
     const int* k0 = kv + kq * DP;
     const int* k1 = kv + (kq + 16) * DP;
-    for (int d = 0; d < a.D; ++d) {
-      const long long x0 = k0[d], x1 = k1[d];
+    // four dimensions per step (16-byte loads; rows 16-byte aligned, zero-padded);
+    // 32 x 32 -> 64-bit products, exact, summed in 64 bits
+    for (int d = 0; d < a.D; d += 4) {
+      const int4 x0 = *reinterpret_cast<const int4*>(k0 + d);
+      const int4 x1 = *reinterpret_cast<const int4*>(k1 + d);
 #pragma unroll
       for (int y = 0; y < 8; ++y) {
         if (y < nh) {
-          const long long qy = qv[(hq + 16 * y) * DP + d];
-          acc[0][y] += x0 * qy;
-          acc[1][y] += x1 * qy;
+          const int4 qy = *reinterpret_cast<const int4*>(qv + (hq + 16 * y) * DP + d);
+          acc[0][y] += (long long)x0.x * qy.x + (long long)x0.y * qy.y + (long long)x0.z * qy.z +
+                       (long long)x0.w * qy.w;
+          acc[1][y] += (long long)x1.x * qy.x + (long long)x1.y * qy.y + (long long)x1.z * qy.z +
+                       (long long)x1.w * qy.w;
         }
       }
     }
@@ -337,6 +357,10 @@ size_t indexer_workspace_bytes(int T, int max_keys) {
   return 256 + (size_t)(T > 0 ? T : 1) * (size_t)(max_keys > 0 ? max_keys : 1) * 8;
 }
 
+size_t indexer_scores_smem(int H, int D) {
+  return idx::dots_offset(H, D) + (size_t)idx::kKeysPerBlock * H * 8;
+}
+
 cudaError_t launch_indexer(int H, int D, int ps, int num_pages, int B, int T, int mask, int window, int top_k,
                            const uint8_t* q, const float* q_s, const uint32_t* offsets, const uint8_t* k,
                            const float* k_scales, const int32_t* block_table, int bt_stride,
@@ -366,8 +390,7 @@ cudaError_t launch_indexer(int H, int D, int ps, int num_pages, int B, int T, in
   a.out_rows = out_rows;
   a.out_scores = out_scores;
   if (T == 0) return cudaSuccess;
-  const size_t s1 = ((((size_t)H + idx::kKeysPerBlock) * (D + 1) * 4 + H + idx::kKeysPerBlock + 15) & ~(size_t)15) +
-                    (size_t)idx::kKeysPerBlock * H * 8;
+  const size_t s1 = indexer_scores_smem(H, D);
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(idx::scores_kernel), (int)s1);
   if (e != cudaSuccess) return e;
   dim3 g1(T, (max_keys + idx::kKeysPerBlock - 1) / idx::kKeysPerBlock);

@@ -70,6 +70,8 @@ cudaError_t launch_prologue(const mla_dims_t& d, void* q, const uint32_t* offset
 
 // The FP8 indexer: exact scores into the workspace, then per-token top_k selection.
 size_t indexer_workspace_bytes(int T, int max_keys);
+// Dynamic shared memory of the scores kernel for H heads of D dimensions.
+size_t indexer_scores_smem(int H, int D);
 cudaError_t launch_indexer(int H, int D, int ps, int num_pages, int B, int T, int mask, int window, int top_k,
                            const uint8_t* q, const float* q_s, const uint32_t* offsets, const uint8_t* k,
                            const float* k_scales, const int32_t* block_table, int bt_stride,

@@ -17,13 +17,14 @@
 //     result is the exactly rounded value of x0 c - x1 s (x0 s + x1 c), as a
 //     double-precision evaluation gives it;
 //   - RMSNorm: the mean square, 1 / sqrt(mean + eps) and the two products are
-//     double precision; the mean square is summed by a tree (the double-precision
-//     sums of any order differ in the last bits only, far below the bf16 rounding
+//     double precision; the mean square is summed by a tree and 1 / sqrt comes
+//     from the double-precision rsqrt (both within a few units of the last place
+//     of the in-order, correctly rounded evaluation, far below the bf16 rounding
 //     step), the products rounded on their own, the result rounded once to bf16.
 //
 // A token's heads are shared by G blocks (blockIdx.y = 0 .. G-1, G chosen so the
-// grid covers the SMs about twice); block 0 of each token also normalises the
-// cache row.
+// grid fills the SMs' resident block slots in one wave); block 0 of each token
+// also normalises the cache row.
 // Each thread loads a batch of its rotation pairs before it stores any (the
 // compiler cannot tell that q and the tables do not overlap, so a loop that
 // loads, turns and stores one pair at a time waits out a global-memory round
@@ -112,6 +113,12 @@ __device__ __forceinline__ void two_sum(float a, float b, float& hi, float& lo) 
   lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, z)), __fsub_rn(b, z));
 }
 
+// bf16 pair (low half first) as two floats.
+__device__ __forceinline__ void bf2(uint32_t v, float& lo, float& hi) {
+  lo = __uint_as_float(v << 16);
+  hi = __uint_as_float(v & 0xFFFF0000u);
+}
+
 // (x0, x1) turned by (c, s), as bf16 bits: the products of bf16 values are
 // exact in fp32.
 __device__ __forceinline__ void rotate(float x0, float x1, float c, float s, uint16_t& y0, uint16_t& y1) {
@@ -135,6 +142,21 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   for (int j = 0; j < kLatPerThread; ++j) {
     const int l = tid + j * kThreads;
     g[j] = row_block && l < a.L ? bf(a.gamma[l]) : 0.0;
+  }
+  // this block's heads [h0, h1) of the query's rope part: pair i = (head h0 + i / (R/2),
+  // pair i % (R/2)), at an even element offset (4-byte aligned, checked by the entry point)
+  const int half = a.R / 2;
+  const int h0 = (int)((long long)blockIdx.y * a.H / gridDim.y), h1 = (int)((long long)(blockIdx.y + 1) * a.H / gridDim.y);
+  const int npairs = (h1 - h0) * half;
+  auto qpair = [&](int i) {
+    return reinterpret_cast<uint32_t*>(a.q + ((size_t)t * a.H + h0 + i / half) * (a.N + a.R) + a.N + 2 * (i % half));
+  };
+  // the first batch of pairs needs no request: its loads go out before the lookup
+  uint32_t xw[kBatch];
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) {
+    const int i = tid + j * kThreads;
+    xw[j] = i < npairs ? *qpair(i) : 0u;
   }
   // the token's request: the b with offsets[b] <= t < offsets[b + 1], found by every
   // thread testing its own b (one round trip instead of a search's log2(B))
@@ -164,15 +186,10 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
     if (tid == 0) atomicOr(&a.hdr->status, kDeviceCheckFailed);
     return;
   }
-  // the page of the row (needed for the row's loads) and the query's first pairs go
-  // out together; a bad page skips the token whole, before anything is written
+  // the page of the row (needed for the row's loads) and the rotation table go out
+  // together; a bad page skips the token whole, before anything is written
   const int page = a.block_table[(size_t)b * a.bt_stride + pos / a.ps];
   const __nv_bfloat16* f = a.freqs + (size_t)pos * a.R;
-  // the query's rope part, this block's heads [h0, h1): pair i = (head h0 + i / (R/2),
-  // pair i % (R/2))
-  const int half = a.R / 2;
-  const int h0 = (int)((long long)blockIdx.y * a.H / gridDim.y), h1 = (int)((long long)(blockIdx.y + 1) * a.H / gridDim.y);
-  const int npairs = (h1 - h0) * half;
   bool page_checked = false;
   for (int i0 = tid; i0 < npairs || !page_checked; i0 += kThreads * kBatch) {
     float x0[kBatch], x1[kBatch], c[kBatch], sn[kBatch];
@@ -180,12 +197,8 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
     for (int j = 0; j < kBatch; ++j) {
       const int i = i0 + j * kThreads;
       if (i < npairs) {
-        const int h = h0 + i / half, pr = i % half;
-        const __nv_bfloat16* x = a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr;
-        x0[j] = bff(x[0]);
-        x1[j] = bff(x[1]);
-        c[j] = bff(f[2 * pr]);
-        sn[j] = bff(f[2 * pr + 1]);
+        bf2(i0 == tid ? xw[j] : *qpair(i), x0[j], x1[j]);
+        bf2(*reinterpret_cast<const uint32_t*>(f + 2 * (i % half)), c[j], sn[j]);
       }
     }
     if (!page_checked) {
@@ -199,12 +212,9 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
     for (int j = 0; j < kBatch; ++j) {
       const int i = i0 + j * kThreads;
       if (i < npairs) {
-        const int h = h0 + i / half, pr = i % half;
-        __nv_bfloat16* x = a.q + ((size_t)t * a.H + h) * (a.N + a.R) + a.N + 2 * pr;
         uint16_t y0, y1;
         rotate(x0[j], x1[j], c[j], sn[j], y0, y1);
-        x[0] = __ushort_as_bfloat16(y0);
-        x[1] = __ushort_as_bfloat16(y1);
+        *qpair(i) = (uint32_t)y0 | ((uint32_t)y1 << 16);
       }
     }
   }
@@ -233,7 +243,9 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const Args a) {
   if (tid == 0) {
     double ms = 0.0;
     for (int w = 0; w < kThreads / 32; ++w) ms = __dadd_rn(ms, s_part[w]);
-    s_inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ms, (double)a.L), a.eps)));
+    // mean: a multiply when L is a power of two (exact), else a division
+    const double mean = (a.L & (a.L - 1)) == 0 ? __dmul_rn(ms, 1.0 / (double)a.L) : __ddiv_rn(ms, (double)a.L);
+    s_inv = rsqrt(__dadd_rn(mean, a.eps));
   }
   __syncthreads();
   const double inv = s_inv;
@@ -283,11 +295,12 @@ cudaError_t launch_prologue(const mla_dims_t& d, void* q, const uint32_t* offset
   a.freqs = static_cast<const __nv_bfloat16*>(freqs);
   a.gamma = static_cast<const __nv_bfloat16*>(gamma);
   a.hdr = hdr;
-  // blocks per token: the grid covers the SMs about twice, at least one head each
+  // blocks per token: the grid fills the SMs' resident slots, at least one head each
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorInvalidDevice;
-  int G = (2 * sms + T - 1) / T;
+  // two blocks per SM are resident (registers): a single wave of at most 2 x SMs blocks
+  int G = (2 * sms) / T;
   if (G > a.H) G = a.H;
   if (G > 65535) G = 65535;
   if (G < 1) G = 1;

@@ -128,6 +128,16 @@ def test_fp8_row_scales_must_be_16_byte_aligned(lib):
     assert rc == 1
 
 
+def test_prologue_pointers_must_be_4_byte_aligned(lib):
+    # rotation pairs are read and written as 4-byte words
+    def call(q=FAKE, pool=FAKE, freqs=FAKE):
+        return lib.mla_branch_prologue(ctypes.byref(_dims()), q, FAKE, 2, 2, pool, FAKE, 4, FAKE, freqs, 8,
+                                       FAKE, 1e-6, 0, FAKE, 1 << 20, None)
+    assert call(q=FAKE + 2) == 1
+    assert call(pool=FAKE + 2) == 1
+    assert call(freqs=FAKE + 2) == 1
+
+
 def _expected_workspace(H, L, R, T, K, NI=1):
     """The workspace sections in order, each starting on a 256-byte boundary:
     plan header, TokenPlan[T] (48 bytes), counters int[T, 4], bounds int[2K + 1],
