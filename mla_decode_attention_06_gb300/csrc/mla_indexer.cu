@@ -34,6 +34,7 @@ namespace mla {
 namespace idx {
 
 constexpr int kKeysPerBlock = 32;
+constexpr int kMaxIndexHeads = 128;   // heads per call (checked by the entry point)
 
 // Row pitch (ints) of the staged query and key values: D rounded up to a multiple
 // of 4 (16-byte loads, rows 16-byte aligned), plus 4 more when that is a multiple
@@ -133,9 +134,13 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
   uint8_t* knan = qnan + a.H;                                            // [32]
   long long* dots = reinterpret_cast<long long*>(sm + dots_offset(a.H, a.D));
   __shared__ long long rows_s[kKeysPerBlock];
+  __shared__ double qs18[kMaxIndexHeads];   // q_s[h] x 2^-18, exact: the dots' unit folded in
   __shared__ int bad_s;
   if (tid == 0) bad_s = 0;
-  for (int i = tid; i < a.H; i += kScoreThreads) qnan[i] = 0;
+  for (int i = tid; i < a.H; i += kScoreThreads) {
+    qnan[i] = 0;
+    qs18[i] = __dmul_rn((double)a.q_s[(size_t)t * a.H + i], 0x1p-18);
+  }
   // padding columns [D, DP) of every row hold zeros (the inner loop reads 4 at a time)
   for (int i = tid; i < (a.H + kKeysPerBlock) * (DP - a.D); i += kScoreThreads)
     qv[(i / (DP - a.D)) * DP + a.D + i % (DP - a.D)] = 0;
@@ -210,9 +215,10 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
       const double ksc = (double)a.k_scales[row];
       double s = 0.0;
       bool nan = knan[tid] != 0;
+      // (q_s ksc) (dot 2^-18) as (q_s 2^-18 ksc) dot: both factors exact either way,
+      // so the one rounded product is the same double
       for (int h = 0; h < a.H; ++h) {
-        const double dot = __dmul_rn((double)dots[tid * a.H + h], 0x1p-18);   // exact
-        s = __dadd_rn(s, __dmul_rn(__dmul_rn((double)a.q_s[(size_t)t * a.H + h], ksc), dot));
+        s = __dadd_rn(s, __dmul_rn(__dmul_rn(qs18[h], ksc), (double)dots[tid * a.H + h]));
         nan = nan || qnan[h];
       }
       if (nan) s = __longlong_as_double(0x7FF8000000000000ll);
