@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
   uint8_t* knan = qnan + a.H;                                            // [32]
   long long* dots = reinterpret_cast<long long*>(sm + dots_offset(a.H, a.D));
   __shared__ long long rows_s[kKeysPerBlock];
+  __shared__ double ksc_s[kKeysPerBlock];   // the keys' row scales
   __shared__ double qs18[kMaxIndexHeads];   // q_s[h] x 2^-18, exact: the dots' unit folded in
   __shared__ int bad_s;
   if (tid == 0) bad_s = 0;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
     if (page >= 0 && page < a.num_pages) row = (long long)page * a.ps + j % a.ps;
     else bad_s = 1;
     rows_s[tid] = row;
+    ksc_s[tid] = row >= 0 ? (double)a.k_scales[row] : 0.0;
   }
   __syncthreads();
   for (int i = tid; i < kKeysPerBlock * a.D; i += kScoreThreads) {
@@ -196,11 +198,15 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
         }
       }
     }
+    // each term of the head sum, (q_s 2^-18 ksc) dot, rounded once (both factors
+    // exact), by the thread that holds the dot; the sum itself runs in head order below
+    double* terms = reinterpret_cast<double*>(dots);
 #pragma unroll
     for (int y = 0; y < 8; ++y) {
       if (y < nh) {
-        dots[kq * a.H + hq + 16 * y] = acc[0][y];
-        dots[(kq + 16) * a.H + hq + 16 * y] = acc[1][y];
+        const int h = hq + 16 * y;
+        terms[kq * a.H + h] = __dmul_rn(__dmul_rn(qs18[h], ksc_s[kq]), (double)acc[0][y]);
+        terms[(kq + 16) * a.H + h] = __dmul_rn(__dmul_rn(qs18[h], ksc_s[kq + 16]), (double)acc[1][y]);
       }
     }
   }
@@ -212,13 +218,13 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
     if (row < 0) {
       key = kInvalidKey;
     } else {
-      const double ksc = (double)a.k_scales[row];
+      // (q_s ksc) (dot 2^-18) was formed as (q_s 2^-18 ksc) dot: both factors exact
+      // either way, so the one rounded product is the same double
+      const double* terms = reinterpret_cast<const double*>(dots);
       double s = 0.0;
       bool nan = knan[tid] != 0;
-      // (q_s ksc) (dot 2^-18) as (q_s 2^-18 ksc) dot: both factors exact either way,
-      // so the one rounded product is the same double
       for (int h = 0; h < a.H; ++h) {
-        s = __dadd_rn(s, __dmul_rn(__dmul_rn(qs18[h], ksc), (double)dots[tid * a.H + h]));
+        s = __dadd_rn(s, terms[tid * a.H + h]);
         nan = nan || qnan[h];
       }
       if (nan) s = __longlong_as_double(0x7FF8000000000000ll);
