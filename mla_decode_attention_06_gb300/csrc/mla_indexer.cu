@@ -35,6 +35,9 @@ namespace idx {
 
 constexpr int kKeysPerBlock = 32;
 constexpr int kMaxIndexHeads = 128;   // heads per call (checked by the entry point)
+constexpr size_t kSelectKeySmem = 160 * 1024;   // the select kernel stages up to this many key bytes
+// Byte offset of the staged keys after the sort buffers (16-byte aligned).
+__host__ __device__ inline size_t select_keys_offset(int sort_n) { return ((size_t)sort_n * 12 + 15) & ~(size_t)15; }
 
 // Row pitch (ints) of the staged query and key values: D rounded up to a multiple
 // of 4 (16-byte loads, rows 16-byte aligned), plus 4 more when that is a multiple
@@ -62,6 +65,7 @@ struct Args {
   const int32_t* block_table;    // [B, bt_stride]
   const uint32_t* cache_lens;    // [B]
   unsigned long long* keys;      // workspace [T, max_keys]
+  bool keys_in_smem;             // select: the launch gave room to stage max_keys keys
   int32_t* out_rows;             // [T, top_k]
   double* out_scores;            // [T, top_k] or NULL
   PlanHeader* hdr;
@@ -239,6 +243,8 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const Args a, in
   extern __shared__ __align__(16) uint8_t sm[];
   unsigned long long* ck = reinterpret_cast<unsigned long long*>(sm);   // [sort_n] candidate keys
   int* cj = reinterpret_cast<int*>(ck + sort_n);                          // [sort_n] their positions
+  // the token's keys, staged once when the launch gave room for max_keys of them
+  unsigned long long* ks = reinterpret_cast<unsigned long long*>(sm + select_keys_offset(sort_n));
   __shared__ unsigned int hist[256];
   __shared__ unsigned long long s_prefix;
   __shared__ int s_need, s_count, s_eq_base[kSelectThreads / 32];
@@ -247,6 +253,11 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const Args a, in
   const bool ok = token_range(a, t, b, lo, hi);
   const int n = ok ? hi - lo : 0;
   const unsigned long long* keys = a.keys + (size_t)t * a.max_keys;
+  if (a.keys_in_smem) {
+    for (int i = tid; i < n; i += kSelectThreads) ks[i] = keys[i];
+    __syncthreads();
+    keys = ks;
+  }
   unsigned long long tau = kInvalidKey;
   int need = n;   // keys equal to tau to take (all keys when n <= K)
   if (n > K) {
@@ -263,15 +274,41 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(const Args a, in
         if (match) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        unsigned int cum = 0;
-        int bin = 0;
-        for (; bin < 255; ++bin) {
-          if (cum + hist[bin] >= (unsigned int)kk) break;
-          cum += hist[bin];
+      // the first bin whose running count reaches kk (bin 255 if none does): warp 0,
+      // eight bins per lane, a warp scan of the lanes' sums, then the crossing lane
+      if (tid < 32) {
+        unsigned int h[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          h[j] = hist[8 * tid + j];
+          sum += h[j];
         }
-        s_prefix = prefix | ((unsigned long long)bin << shift);
-        s_need = kk - (int)cum;
+        unsigned int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += v;
+        }
+        const unsigned int hit = __ballot_sync(0xffffffffu, incl >= (unsigned int)kk);
+        const int L = hit ? __ffs(hit) - 1 : 31;
+        if (tid == L) {
+          unsigned int cum = incl - sum;
+          int bin = 8 * L;
+          bool done = false;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (!done) {
+              if (bin == 255 || cum + h[j] >= (unsigned int)kk) {
+                done = true;
+              } else {
+                cum += h[j];
+                ++bin;
+              }
+            }
+          }
+          s_prefix = prefix | ((unsigned long long)bin << shift);
+          s_need = kk - (int)cum;
+        }
       }
       __syncthreads();
       prefix = s_prefix;
@@ -410,10 +447,11 @@ cudaError_t launch_indexer(int H, int D, int ps, int num_pages, int B, int T, in
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   int sort_n = 1;
   while (sort_n < top_k) sort_n <<= 1;
-  const size_t s2 = (size_t)sort_n * 12;
+  a.keys_in_smem = (size_t)max_keys * 8 <= idx::kSelectKeySmem;
+  const size_t s2 = idx::select_keys_offset(sort_n) + (a.keys_in_smem ? (size_t)max_keys * 8 : 0);
   e = ensure_smem_limit(reinterpret_cast<const void*>(idx::select_kernel), (int)s2);
   if (e != cudaSuccess) return e;
-  idx::select_kernel<<<T, idx::kSelectThreads, s2, s>>>(a, sort_n);
+  idx::select_kernel<<<T, idx::kSelectThreads, s2, s>>>(a, sort_n);   // a.keys_in_smem set above
   return cudaGetLastError();
 }
 
