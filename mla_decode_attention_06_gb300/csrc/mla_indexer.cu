@@ -151,11 +151,14 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
     qv[(i / (DP - a.D)) * DP + a.D + i % (DP - a.D)] = 0;
   if (tid < kKeysPerBlock) knan[tid] = 0;
   __syncthreads();
-  for (int i = tid; i < HD; i += kScoreThreads) {
-    const uint32_t c = a.q[(size_t)t * HD + i];
-    qv[(i / a.D) * DP + i % a.D] = e4m3_times_512(c);
-    if (e4m3_is_nan(c)) qnan[i / a.D] = 1;
-  }
+  // a warp per head, a lane per dimension (no division per element)
+  const int wid = tid >> 5, lane = tid & 31;
+  for (int h = wid; h < a.H; h += kScoreThreads / 32)
+    for (int d = lane; d < a.D; d += 32) {
+      const uint32_t c = a.q[(size_t)t * HD + h * a.D + d];
+      qv[h * DP + d] = e4m3_times_512(c);
+      if (e4m3_is_nan(c)) qnan[h] = 1;
+    }
   if (tid < nk) {
     const int j = lo + j0 + tid;
     const int page = a.block_table[(size_t)b * a.bt_stride + j / a.ps];
@@ -166,12 +169,14 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
     ksc_s[tid] = row >= 0 ? (double)a.k_scales[row] : 0.0;
   }
   __syncthreads();
-  for (int i = tid; i < kKeysPerBlock * a.D; i += kScoreThreads) {
-    const int key = i / a.D, d = i % a.D;
+  // a warp per key, a lane per dimension
+  for (int key = wid; key < kKeysPerBlock; key += kScoreThreads / 32) {
     const long long row = key < nk ? rows_s[key] : -1;
-    const uint32_t c = row >= 0 ? a.k[(size_t)row * a.D + d] : 0u;
-    kv[key * DP + d] = e4m3_times_512(c);
-    if (key < nk && e4m3_is_nan(c)) knan[key] = 1;
+    for (int d = lane; d < a.D; d += 32) {
+      const uint32_t c = row >= 0 ? a.k[(size_t)row * a.D + d] : 0u;
+      kv[key * DP + d] = e4m3_times_512(c);
+      if (key < nk && e4m3_is_nan(c)) knan[key] = 1;
+    }
   }
   __syncthreads();
   // exact inner products in units of 2^-18 (each product below 2^36, sums in 64 bits):
@@ -203,14 +208,15 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
       }
     }
     // each term of the head sum, (q_s 2^-18 ksc) dot, rounded once (both factors
-    // exact), by the thread that holds the dot; the sum itself runs in head order below
+    // exact), by the thread that holds the dot; the sum itself runs in head order below.
+    // Rows of H + 1 doubles: the adding warp's 32 lanes (one key each) read 32 banks.
     double* terms = reinterpret_cast<double*>(dots);
 #pragma unroll
     for (int y = 0; y < 8; ++y) {
       if (y < nh) {
         const int h = hq + 16 * y;
-        terms[kq * a.H + h] = __dmul_rn(__dmul_rn(qs18[h], ksc_s[kq]), (double)acc[0][y]);
-        terms[(kq + 16) * a.H + h] = __dmul_rn(__dmul_rn(qs18[h], ksc_s[kq + 16]), (double)acc[1][y]);
+        terms[kq * (a.H + 1) + h] = __dmul_rn(__dmul_rn(qs18[h], ksc_s[kq]), (double)acc[0][y]);
+        terms[(kq + 16) * (a.H + 1) + h] = __dmul_rn(__dmul_rn(qs18[h], ksc_s[kq + 16]), (double)acc[1][y]);
       }
     }
   }
@@ -228,7 +234,7 @@ __global__ void __launch_bounds__(kScoreThreads) scores_kernel(const Args a) {
       double s = 0.0;
       bool nan = knan[tid] != 0;
       for (int h = 0; h < a.H; ++h) {
-        s = __dadd_rn(s, terms[tid * a.H + h]);
+        s = __dadd_rn(s, terms[tid * (a.H + 1) + h]);
         nan = nan || qnan[h];
       }
       if (nan) s = __longlong_as_double(0x7FF8000000000000ll);
@@ -407,7 +413,7 @@ size_t indexer_workspace_bytes(int T, int max_keys) {
 }
 
 size_t indexer_scores_smem(int H, int D) {
-  return idx::dots_offset(H, D) + (size_t)idx::kKeysPerBlock * H * 8;
+  return idx::dots_offset(H, D) + (size_t)idx::kKeysPerBlock * (H + 1) * 8;
 }
 
 cudaError_t launch_indexer(int H, int D, int ps, int num_pages, int B, int T, int mask, int window, int top_k,
