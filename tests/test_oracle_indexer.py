@@ -3,7 +3,7 @@
 score = sum over heads of q_s * k_scale * (q . k), masked like the decode, -1 past
 the number of keys.  Each pin checks the oracle against something other than
 itself: a pure-Python brute force over torch's e4m3 decoder, an independent
-vectorised formulation judged by the properties that define a top-k, closed forms,
+vectorised formulation checked against the properties that define a top-k, closed forms,
 invariants and the masks.  CPU only.
 """
 import numpy as np
