@@ -136,6 +136,23 @@ def test_fp8_small(dev, num_splits):
                      lens=(5, 64, 300, 900)), dev, num_splits=num_splits)
 
 
+@pytest.mark.parametrize("ps", [8, 16, 32])
+def test_fp8_small_pages(dev, ps):
+    # a page load of ps < 64 rows brings ps row scales (32-128 bytes) into shared memory
+    lens = (5, 64, 300, 900)
+    pages = sum((n + ps - 1) // ps for n in lens) + 16
+    check(dsv3_small(name=f"fp8_ps{ps}", kv_fmt="fp8", w_fmt="fp8", rms_norm=False, ps=ps, lens=lens,
+                     num_pages=pages), dev, num_splits=3)
+
+
+def test_fp8_narrow_latent(dev):
+    # latent 64 (one CTA per partition): the codes share box 0 with the widened values
+    p = W.make_dense("fp8_narrow", 41, H=4, N=32, R=16, L=64, V=32, ps=16, cache_lens=[37, 70, 5, 130],
+                     num_pages=24, mask=W.MASK_CAUSAL, kv_fmt="fp8", w_fmt="fp8")
+    check(p, dev)
+    check(p, dev, num_splits=4)
+
+
 @pytest.mark.parametrize("num_splits", [0, 1, 5])
 def test_sparse_small(dev, num_splits):
     p = W.make_sparse("sparse_small", 31, **DSV3, ps=64, tokens_per_request=4096,
