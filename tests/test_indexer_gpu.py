@@ -69,6 +69,14 @@ def test_deepseek_shaped_selection(dev):
     assert (rows == -1).any() and (rows[:, -1] >= 0).any()
 
 
+@pytest.mark.parametrize("D", [22, 5])
+def test_head_dim_not_a_multiple_of_four(dev, D):
+    # the staged rows are zero-padded to a multiple of 4 dimensions (16-byte loads)
+    p = make_indexer(f"idx_gpu_d{D}", 17 + D, H=5, D=D, ps=16, cache_lens=[50, 130, 9], top_k=40,
+                     num_pages=32)
+    _check(p, dev)
+
+
 def test_equal_scores_keep_key_order(dev):
     p = make_indexer("idx_gpu_ties", 7, H=3, D=16, ps=8, cache_lens=[300, 5, 1000], top_k=100,
                      num_pages=200)
