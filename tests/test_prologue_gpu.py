@@ -60,10 +60,16 @@ def _expected(p, freqs, gamma, pool_h):
     return q2, phys
 
 
-@pytest.mark.parametrize("case", ["tiny", "dsv3_multi_token", "dsv3_page16"])
+@pytest.mark.parametrize("case", ["tiny", "dsv3_multi_token", "dsv3_page16", "many_tokens"])
 def test_prologue_is_bit_exact(dev, case):
     if case == "tiny":
         p = W.config_tiny()
+    elif case == "many_tokens":
+        # more tokens than two per SM: one block per token (the other cases split a
+        # token's heads over several blocks)
+        lens = [int(x) for x in W.Stream(64, "prologue-many").integers(1, 200, 400)]
+        p = W.make_dense("prologue_many", 64, H=4, N=32, R=16, L=64, V=32, ps=16, cache_lens=lens,
+                         num_pages=sum((n + 15) // 16 for n in lens) + 8)
     elif case == "dsv3_multi_token":
         p = W.make_dense("prologue_mt", 61, **W.DSV3, ps=64, cache_lens=[5, 300, 4100, 64],
                          qlens=[1, 2, 3, 1], num_pages=128, rms_norm=True)
