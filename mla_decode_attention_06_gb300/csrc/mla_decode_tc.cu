@@ -228,11 +228,18 @@ __device__ __forceinline__ void tma_gather4_mc(void* dst, const CUtensorMap* map
       : "memory");
 }
 
-// Two e4m3 codes times a row scale, rounded to a bf16 pair (low half = first code).
+// Two e4m3 codes times a row scale, rounded to a bf16 pair (low half = first code):
+// the codes widen exactly (through f16), one packed fp32 multiply (round to
+// nearest, per lane as two scalar ones) scales both, one conversion rounds both.
 __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint16_t two, float scale) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
   const float2 f = __half22float2(__half2(h));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+  float x, y;
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %4};\n\tmul.rn.f32x2 d, a, b;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(x), "=f"(y)
+      : "f"(f.x), "f"(f.y), "f"(scale));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(x, y);
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
@@ -972,21 +979,31 @@ __global__ void __launch_bounds__(Cfg<LC, CL, MODE>::kThreads, 1)
             mbar_arrive(&cs->conv_sync);
             if (!wwait(&cs->conv_sync, c & 1, cs, hdr)) return;
           }
-#pragma unroll
-          for (int q = 0; q < kChunks; ++q) {
-            const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
-            uint32_t o[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              o[2 * i] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc) : 0u;
-              o[2 * i + 1] = live ? e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc) : 0u;
-            }
-            // first latent column of the chunk
-            const int col = p * C::RW + hh * kPart + 16 * ((q + crow) & (kChunks - 1));
+          // chunk q's 16 widened columns go to two 16-byte slots of the swizzled box row
+          auto put = [&](int q, const uint32_t (&o)[8]) {
+            const int col = p * C::RW + hh * kPart + 16 * ((q + crow) & (kChunks - 1));   // its first column
             uint8_t* box = st + (col >> 6) * C::kBox + crow * 128;
             const int ch = (col & 63) >> 3;          // 16-byte chunk within the 128-byte row
             *reinterpret_cast<uint4*>(box + (((ch) ^ (crow & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<uint4*>(box + (((ch + 1) ^ (crow & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          };
+          if (live) {
+#pragma unroll
+            for (int q = 0; q < kChunks; ++q) {
+              const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+              uint32_t o[8];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                o[2 * i] = e4m3x2_scaled_bf16x2((uint16_t)(w[i] & 0xffff), sc);
+                o[2 * i + 1] = e4m3x2_scaled_bf16x2((uint16_t)(w[i] >> 16), sc);
+              }
+              put(q, o);
+            }
+          } else {
+            // a dead row (only in a token's ragged tiles) becomes zeros
+            const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int q = 0; q < kChunks; ++q) put(q, z);
           }
           if (C::NRH > 1 && p == 0) {
             // latent [0, RW) is in place: the QK's TMEM-operand part may start
